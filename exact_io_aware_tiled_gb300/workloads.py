@@ -1,0 +1,109 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module only draws random numbers and rounds them to the storage dtype;
+it holds none of the attention arithmetic.  Tests, the benchmark and the
+oracle-side checks all take their inputs from here, so both sides of a parity
+comparison see bit-identical values.
+
+Recipe (shapes follow the workloads the FlashAttention pages measure or
+discuss: GPT-2-medium attention B=64, H=16, N=1024, d=64 and BERT-large at
+N=512 -- agihunt.info summary of arXiv 2205.14135, results paragraph and
+table; a 23,400-step day with 12 heads in fp16 -- marketmaker.cc,
+introduction; butterfly block-sparse attention to 64K -- agihunt.info,
+block-sparse paragraph):
+
+* one ``numpy.random.Generator`` per tensor: ``default_rng([seed, stream])``
+  with streams 0..3 for Q, K, V, dO;
+* i.i.d. N(0, 1) drawn in float32, multiplied by ``input_scale``, then rounded
+  to the storage dtype with round-to-nearest-even (torch CPU casts);
+* key-padding lengths L_b = integers(lo, hi + 1) from stream 4;
+* block-sparse: kept(I, J) iff I == J or I ^ J is a power of two over
+  N / 128 blocks.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Optional
+
+import numpy as np
+import torch
+
+DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def butterfly(nblocks: int) -> np.ndarray:
+    i = np.arange(nblocks)[:, None]
+    j = np.arange(nblocks)[None, :]
+    x = i ^ j
+    return ((x == 0) | ((x & (x - 1)) == 0)).astype(np.uint8)
+
+
+@dataclass
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int = 64
+    dtype: str = "bf16"
+    causal: bool = False
+    seqlen_range: Optional[tuple] = None      # (lo, hi) inclusive, or None
+    sparse_butterfly: bool = False
+    block_size: int = 128
+    dropout_p: float = 0.0
+    dropout_seed: int = 0x5EED
+    dropout_offset: int = 0
+    input_scale: float = 1.0
+    seed: int = 20260
+    seqlens: Optional[np.ndarray] = field(default=None, repr=False)
+    block_mask: Optional[np.ndarray] = field(default=None, repr=False)
+
+    def __post_init__(self):
+        if self.seqlen_range is not None and self.seqlens is None:
+            lo, hi = self.seqlen_range
+            rng = np.random.default_rng([self.seed, 4])
+            self.seqlens = rng.integers(lo, hi + 1, size=self.B).astype(np.int32)
+        if self.sparse_butterfly and self.block_mask is None:
+            nb = -(-self.N // self.block_size)
+            self.block_mask = butterfly(nb)
+
+    @property
+    def torch_dtype(self):
+        return DTYPES[self.dtype]
+
+    def with_(self, **kw):
+        return replace(self, **kw)
+
+
+def _draw(shape, seed, stream, scale, dtype):
+    rng = np.random.default_rng([seed, stream])
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if scale != 1.0:
+        x = x * np.float32(scale)
+    return torch.from_numpy(x).to(DTYPES[dtype])
+
+
+def make_inputs(wl: Workload, grads: bool = True):
+    """q, k, v (and do) as torch CPU tensors of the storage dtype, [B,H,N,d]."""
+    shp = (wl.B, wl.H, wl.N, wl.d)
+    out = {n: _draw(shp, wl.seed, s, wl.input_scale, wl.dtype)
+           for s, n in enumerate(("q", "k", "v"))}
+    if grads:
+        out["do"] = _draw(shp, wl.seed, 3, wl.input_scale, wl.dtype)
+    return out
+
+
+# The five workloads (name -> Workload).  Seeds are 20260 + index.
+CONFIGS = {
+    "tiny_f32": Workload("tiny_f32", B=1, H=2, N=256, dtype="f32", seed=20261),
+    "gpt2_medium_causal": Workload("gpt2_medium_causal", B=64, H=16, N=1024,
+                                   dtype="bf16", causal=True, seed=20262),
+    "bert_large_pad_dropout": Workload("bert_large_pad_dropout", B=32, H=16, N=512,
+                                       dtype="bf16", seqlen_range=(256, 512),
+                                       dropout_p=0.1, seed=20263),
+    "long_ragged_causal_f16": Workload("long_ragged_causal_f16", B=1, H=12, N=23400,
+                                       dtype="f16", causal=True, input_scale=0.5,
+                                       seed=20264),
+    "butterfly_sparse_64k": Workload("butterfly_sparse_64k", B=1, H=8, N=65536,
+                                     dtype="bf16", sparse_butterfly=True, seed=20265),
+}

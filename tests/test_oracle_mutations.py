@@ -1,0 +1,51 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of ``oracle/`` on the CPU (a dropped
+scale, a flipped sign, a transposed operand, a wrong mask boundary, ...) and
+runs the pin tests against the copy in a subprocess; at least one pin must
+fail.  Nothing here touches a GPU.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = [
+    ("attention.py", "dk += tau * (dS.T @ q[r])", "dk += (dS.T @ q[r])"),
+    ("attention.py", "dS = P * (dP - Dr[:, None])", "dS = P * (dP + Dr[:, None])"),
+    ("attention.py", "dq[s:s + ROW_CHUNK] = tau * (dS @ k)", "dq[s:s + ROW_CHUNK] = tau * (dS @ q[r])"),
+    ("attention.py", "dv += Pt.T @ do[r]", "dv += P.T @ do[r]"),
+    ("attention.py", "dP = Z * dPt / (1.0 - spec.dropout_p)", "dP = dPt"),
+    ("attention.py", "Pt = keep(spec, b, h, r, cols) * P / (1.0 - spec.dropout_p)",
+     "Pt = keep(spec, b, h, r, cols) * P"),
+    ("attention.py", "m_safe + np.log(", "m_safe + np.log1p("),
+    ("masks.py", "m &= cols <= rows", "m &= cols < rows"),
+    ("masks.py", "m &= cols < int(seqlen_k)", "m &= cols <= int(seqlen_k)"),
+    ("tiled.py", "Oi = alpha[:, None] * Oi + P @ v[cj[0]:cj[1]]", "Oi = Oi + P @ v[cj[0]:cj[1]]"),
+    ("tiled.py", "l_new = a_old * li + a_til * P_til.sum(axis=1)", "l_new = li + a_til * P_til.sum(axis=1)"),
+    ("philox.py", "c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0",
+     "c0, c1, c2, c3 = hi0 ^ c1 ^ k0, lo1, hi1 ^ c3 ^ k1, lo0"),
+    ("philox.py", "return half >= np.uint64(T)", "return half > np.uint64(T)"),
+]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("fname,old,new", MUTATIONS)
+def test_pins_catch_planted_mistake(tmp_path, fname, old, new):
+    dst = tmp_path / "r"
+    shutil.copytree(os.path.join(ROOT, "oracle"), dst / "oracle")
+    shutil.copytree(os.path.join(ROOT, "tests"), dst / "tests",
+                    ignore=shutil.ignore_patterns("test_oracle_mutations.py", "__pycache__", "test_gpu*", "test_zz*"))
+    p = dst / "oracle" / fname
+    src = p.read_text()
+    assert src.count(old) == 1, "mutation anchor not found: " + old
+    p.write_text(src.replace(old, new))
+    tests = [str(dst / "tests" / t) for t in ("test_oracle_attention.py", "test_oracle_tiled.py",
+                                             "test_oracle_philox.py", "test_oracle_traffic.py")]
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "-m", "not slow", *tests], cwd=dst, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 1, "planted mistake survived every pin:\n" + r.stdout[-2000:]
