@@ -1,0 +1,10 @@
+"""Exact, IO-aware, tiled attention (FlashAttention) for GB300 (sm_103a).
+
+The computation lives in ``libfa_gb300.so`` (C ABI: include/fa.h): a
+tcgen05/TMA/TMEM forward and backward kernel for bf16/fp16, CUDA-core kernels
+for float32, and small HBM-bound helper kernels.  This package is a thin
+ctypes binding plus the seeded synthetic workload generators.
+"""
+from ._lib import (FAError, bwd, check_status, dropout_mask, fwd, load, make_params,  # noqa: F401
+                   status_string, EXPORTED, DTYPE_CODE)
+from ._build import build, LIB  # noqa: F401

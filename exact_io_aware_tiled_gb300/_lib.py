@@ -1,0 +1,213 @@
+"""ctypes binding of the C ABI in include/fa.h (argument marshalling only).
+
+Every step of the attention computation runs in the CUDA kernels of
+``libfa_gb300.so``; this module only checks tensor shapes and devices, allocates
+outputs and the workspace with torch, and passes raw pointers and the current
+CUDA stream.  If the library has not been built it raises -- there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from pathlib import Path
+from typing import Optional
+
+import torch
+
+_LIB_PATH = Path(__file__).resolve().parent / "libfa_gb300.so"
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_WORKSPACE, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(7)
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+EXPORTED = ["fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd", "fa_check_status",
+            "fa_dropout_mask", "fa_status_string", "fa_version"]
+
+
+class fa_params(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("N", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("stride_b", ctypes.c_int64), ("stride_h", ctypes.c_int64), ("stride_n", ctypes.c_int64),
+        ("scale", ctypes.c_float),
+        ("causal", ctypes.c_int32),
+        ("seqlens_k", ctypes.c_void_p),
+        ("dropout_p", ctypes.c_float),
+        ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
+        ("block_mask", ctypes.c_void_p),
+        ("block_size", ctypes.c_int32),
+        ("o_f32", ctypes.c_void_p),
+    ]
+
+
+class FAError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__("%s: %s" % (what, status_string(code)))
+
+
+_lib = None
+
+
+def load():
+    """Load libfa_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not _LIB_PATH.exists():
+        raise RuntimeError("libfa_gb300.so is not built; run "
+                           "`python -m exact_io_aware_tiled_gb300._build` (or __graft_entry__.build())")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    P = ctypes.POINTER(fa_params)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    lib.fa_fwd_workspace_size.argtypes = [P]
+    lib.fa_fwd_workspace_size.restype = sz
+    lib.fa_bwd_workspace_size.argtypes = [P]
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.fa_fwd.restype = ctypes.c_int
+    lib.fa_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.fa_bwd.restype = ctypes.c_int
+    lib.fa_check_status.argtypes = [vp, vp]
+    lib.fa_check_status.restype = ctypes.c_int
+    lib.fa_dropout_mask.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp]
+    lib.fa_dropout_mask.restype = ctypes.c_int
+    lib.fa_status_string.argtypes = [ctypes.c_int]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = ctypes.c_int32
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().fa_status_string(int(code)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_params(q: torch.Tensor, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0,
+                block_mask=None, scale=None, o_f32=None) -> fa_params:
+    B, H, N, d = q.shape
+    p = fa_params()
+    p.B, p.H, p.N, p.d = B, H, N, d
+    p.dtype = DTYPE_CODE[q.dtype]
+    p.stride_b, p.stride_h, p.stride_n = q.stride(0), q.stride(1), q.stride(2)
+    p.scale = 0.0 if scale is None else float(scale)
+    p.causal = 1 if causal else 0
+    p.seqlens_k = None if seqlens_k is None else seqlens_k.data_ptr()
+    p.dropout_p = float(dropout_p)
+    p.seed = int(seed) & (2 ** 64 - 1)
+    p.offset = int(offset) & (2 ** 64 - 1)
+    p.block_mask = None if block_mask is None else block_mask.data_ptr()
+    p.block_size = 128
+    p.o_f32 = None if o_f32 is None else o_f32.data_ptr()
+    return p
+
+
+def _same_layout(ts):
+    """All [B,H,N,d] tensors must share one stride set with a contiguous last dim."""
+    ref = ts[0]
+    ok = all(t.shape == ref.shape and t.stride() == ref.stride() and t.dtype == ref.dtype for t in ts)
+    ok = ok and ref.stride(3) == 1
+    if ok:
+        return ts
+    return [t.contiguous() for t in ts]
+
+
+def _check(q, name="q"):
+    if q.dim() != 4:
+        raise ValueError("%s must be [B, H, N, d]" % name)
+    if not q.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if q.dtype not in DTYPE_CODE:
+        raise ValueError("unsupported dtype %s" % q.dtype)
+
+
+def _aux(seqlens_k, block_mask, q):
+    B, N = q.shape[0], q.shape[2]
+    if seqlens_k is not None:
+        if tuple(seqlens_k.shape) != (B,):
+            raise ValueError("seqlens_k must have shape [B]")
+        seqlens_k = seqlens_k.to(device=q.device, dtype=torch.int32).contiguous()
+    if block_mask is not None:
+        nb = -(-N // 128)
+        if tuple(block_mask.shape) != (nb, nb):
+            raise ValueError("block_mask must have shape [ceil(N/128), ceil(N/128)] = [%d, %d]" % (nb, nb))
+        block_mask = block_mask.to(device=q.device, dtype=torch.uint8).contiguous()
+    return seqlens_k, block_mask
+
+
+def fwd(q, k, v, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0, block_mask=None,
+        scale=None, return_o_f32=False, stream=None):
+    """O, LSE (and optionally the float32 O before rounding) via fa_fwd."""
+    _check(q)
+    q, k, v = _same_layout([q, k, v])
+    lib = load()
+    seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    o32 = torch.empty((B, H, N, d), device=q.device, dtype=torch.float32) if return_o_f32 else None
+    p = make_params(q, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
+                    block_mask=block_mask, scale=scale, o_f32=o32)
+    wsz = lib.fa_fwd_workspace_size(ctypes.byref(p))
+    ws = torch.empty(wsz, device=q.device, dtype=torch.uint8)
+    st = lib.fa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), wsz, _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd")
+    fwd.last_workspace = ws
+    return (o, lse, o32) if return_o_f32 else (o, lse)
+
+
+def bwd(q, k, v, o, do, lse, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0, block_mask=None,
+        scale=None, stream=None):
+    """dQ, dK, dV via fa_bwd."""
+    _check(q)
+    q, k, v, o, do = _same_layout([q, k, v, o, do])
+    lib = load()
+    seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
+    lse = lse.contiguous()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    p = make_params(q, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
+                    block_mask=block_mask, scale=scale)
+    wsz = lib.fa_bwd_workspace_size(ctypes.byref(p))
+    ws = torch.empty(wsz, device=q.device, dtype=torch.uint8)
+    st = lib.fa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                    _ptr(dv), _ptr(ws), wsz, _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd")
+    bwd.last_workspace = ws
+    return dq, dk, dv
+
+
+def check_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise and return the status word a previous call left in ``ws``."""
+    return load().fa_check_status(_ptr(ws), _stream(stream))
+
+
+def dropout_mask(B, H, N, b, h, row0, nrows, *, dropout_p, seed=0, offset=0, device="cuda", stream=None):
+    """uint8 [nrows, N] keep-mask of rows row0.. of head (b, h) via fa_dropout_mask."""
+    lib = load()
+    p = fa_params()
+    p.B, p.H, p.N, p.d = B, H, N, 64
+    p.dropout_p = float(dropout_p)
+    p.seed = int(seed) & (2 ** 64 - 1)
+    p.offset = int(offset) & (2 ** 64 - 1)
+    out = torch.empty((nrows, N), device=device, dtype=torch.uint8)
+    st = lib.fa_dropout_mask(ctypes.byref(p), b, h, row0, nrows, _ptr(out), _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_dropout_mask")
+    return out
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

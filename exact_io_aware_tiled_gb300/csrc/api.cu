@@ -1,0 +1,303 @@
+// api.cu -- host side of the C ABI declared in include/fa.h.
+//
+// Validates arguments, lays out the caller's workspace, encodes the TMA
+// tensor maps (cuTensorMapEncodeTiled, fetched through the runtime's
+// driver-entry-point query so the library needs no -lcuda), and enqueues the
+// kernels on the caller's stream.  It never allocates, frees or synchronises
+// device memory (fa_check_status excepted) and keeps no mutable global state.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+  size_t status = 0, rlist = 0, rcnt = 0, clist = 0, ccnt = 0, lse2 = 0, dvec = 0, dqacc = 0, total = 0;
+  bool sparse = false;
+  int nb = 0, nq = 0, npad = 0;
+};
+
+Layout layout(const fa_params* p, bool bwd) {
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  L.nq = (p->N + kTile - 1) / kTile;
+  L.npad = L.nq * kTile;
+  L.status = take(256);
+  if (p->block_mask != nullptr) {
+    L.sparse = true;
+    L.nb = L.nq;
+    L.rlist = take((size_t)L.nb * L.nb * sizeof(int16_t));
+    L.rcnt = take((size_t)L.nb * sizeof(int32_t));
+    L.clist = take((size_t)L.nb * L.nb * sizeof(int16_t));
+    L.ccnt = take((size_t)L.nb * sizeof(int32_t));
+  }
+  if (bwd) {
+    const size_t rows = (size_t)p->B * p->H * L.npad;
+    L.lse2 = take(rows * sizeof(float));
+    L.dvec = take(rows * sizeof(float));
+    if (p->dtype != FA_DT_F32) L.dqacc = take((size_t)p->B * p->H * p->N * kHeadDim * sizeof(float));
+  }
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+int elem_bytes(int dt) { return dt == FA_DT_F32 ? 4 : 2; }
+
+// Shape / dtype / stride / alignment checks shared by fa_fwd and fa_bwd.
+fa_status check_params(const fa_params* p) {
+  if (p == nullptr) return FA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->N < 1 || p->d < 1) return FA_ERR_INVALID_ARG;
+  if (p->dtype != FA_DT_F32 && p->dtype != FA_DT_F16 && p->dtype != FA_DT_BF16) return FA_ERR_INVALID_ARG;
+  if (p->d != kHeadDim) return FA_ERR_UNSUPPORTED;
+  if (p->stride_n < p->d || p->stride_h < 1 || p->stride_b < 1) return FA_ERR_INVALID_ARG;
+  if (!(p->dropout_p >= 0.f && p->dropout_p < 1.f)) return FA_ERR_INVALID_ARG;
+  if ((long long)p->B * p->H * p->N >= (1ll << 32)) return FA_ERR_UNSUPPORTED;
+  if (p->block_mask != nullptr && p->block_size != kTile) return FA_ERR_UNSUPPORTED;
+  if (p->block_mask != nullptr && (p->N + kTile - 1) / kTile > 32767) return FA_ERR_UNSUPPORTED;
+  const int64_t unit = 16 / elem_bytes(p->dtype);   // elements per 16 bytes
+  if (p->stride_n % unit || p->stride_h % unit || p->stride_b % unit) return FA_ERR_MISALIGNED;
+  if (p->o_f32 != nullptr && !aligned16(p->o_f32)) return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
+Strides strides_of(const fa_params* p) {
+  // Singleton dimensions carry whatever stride the caller had; normalise them
+  // so every stride handed to TMA is a valid, representable byte stride.
+  Strides s{p->stride_b, p->stride_h, p->stride_n};
+  if (p->H == 1) s.h = (int64_t)p->N * s.n;
+  if (p->B == 1) s.b = (int64_t)p->H * s.h;
+  return s;
+}
+
+float scale_of(const fa_params* p) {
+  return (p->scale > 0.f && std::isfinite(p->scale)) ? p->scale : 1.f / std::sqrt((float)p->d);
+}
+
+DropoutArgs dropout_of(const fa_params* p) {
+  DropoutArgs d{};
+  d.k0 = (uint32_t)(p->seed & 0xFFFFFFFFu);
+  d.k1 = (uint32_t)(p->seed >> 32);
+  d.off_lo = (uint32_t)(p->offset & 0xFFFFFFFFu);
+  d.off_hi = (uint32_t)(p->offset >> 32);
+  const double t = std::floor((double)p->dropout_p * 65536.0 + 0.5);
+  d.threshold = (uint32_t)t;
+  d.rp = 1.f / (1.f - p->dropout_p);
+  d.enabled = p->dropout_p > 0.f ? 1 : 0;
+  return d;
+}
+
+// 4-D map over a [B,H,N,cols] tensor: dims (cols, N, H, B), box (box_c, 128, 1, 1), 128-byte swizzle.
+fa_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int cols, int box_c,
+                   const fa_params* p, Strides s) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return FA_ERR_CUDA;
+  cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)p->N, (cuuint64_t)p->H, (cuuint64_t)p->B};
+  cuuint64_t strides[3] = {(cuuint64_t)(s.n * esize), (cuuint64_t)(s.h * esize), (cuuint64_t)(s.b * esize)};
+  cuuint32_t box[4] = {(cuuint32_t)box_c, (cuuint32_t)kTile, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status map16(CUtensorMap* m, const void* base, const fa_params* p, Strides s) {
+  const CUtensorMapDataType dt =
+      p->dtype == FA_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return make_map(m, base, dt, 2, kHeadDim, kHeadDim, p, s);
+}
+
+MaskArgs mask_of(const fa_params* p, const Layout& L, uint8_t* ws) {
+  MaskArgs m{};
+  m.causal = p->causal ? 1 : 0;
+  m.seqlens_k = p->seqlens_k;
+  if (L.sparse) {
+    m.row_list = reinterpret_cast<const int16_t*>(ws + L.rlist);
+    m.row_cnt = reinterpret_cast<const int32_t*>(ws + L.rcnt);
+    m.col_list = reinterpret_cast<const int16_t*>(ws + L.clist);
+    m.col_cnt = reinterpret_cast<const int32_t*>(ws + L.ccnt);
+    m.nb = L.nb;
+  }
+  return m;
+}
+
+fa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+fa_status prepare_common(const fa_params* p, const Layout& L, uint8_t* ws, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(ws + L.status, 0, sizeof(int), st);
+  if (e == cudaSuccess && L.sparse)
+    e = launch_block_lists(p->block_mask, L.nb, reinterpret_cast<int16_t*>(ws + L.rlist),
+                           reinterpret_cast<int32_t*>(ws + L.rcnt), reinterpret_cast<int16_t*>(ws + L.clist),
+                           reinterpret_cast<int32_t*>(ws + L.ccnt), st);
+  return cuda_status(e);
+}
+
+bool fwd_p_in_tmem() {
+  const char* v = std::getenv("FA_FWD_P_SMEM");
+  return !(v != nullptr && v[0] == '1');
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+size_t fa_fwd_workspace_size(const fa_params* p) {
+  if (p == nullptr || p->N < 1) return 256;
+  return layout(p, false).total;
+}
+
+size_t fa_bwd_workspace_size(const fa_params* p) {
+  if (p == nullptr || p->N < 1 || p->B < 1 || p->H < 1) return 256;
+  return layout(p, true).total;
+}
+
+fa_status fa_fwd(const fa_params* p, const void* q, const void* k, const void* v, void* o, float* lse, void* ws,
+                 size_t ws_bytes, void* stream) {
+  fa_status s = check_params(p);
+  if (s != FA_OK) return s;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
+  const Layout L = layout(p, false);
+  if (ws == nullptr || ws_bytes < L.total || !aligned16(ws)) return FA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const Strides sd = strides_of(p);
+
+  FwdArgs a{};
+  a.B = p->B; a.H = p->H; a.N = p->N;
+  a.nq = L.nq;
+  a.npairs = (L.nq + 1) / 2;
+  a.scale_log2 = scale_of(p) * 1.4426950408889634f;
+  a.mask = mask_of(p, L, w);
+  a.drop = dropout_of(p);
+  a.lse = lse;
+  a.o_f32 = p->o_f32;
+  a.status = reinterpret_cast<int*>(w + L.status);
+
+  if ((s = prepare_common(p, L, w, st)) != FA_OK) return s;
+  if (p->dtype == FA_DT_F32) {
+    if (p->o_f32 != nullptr) return FA_ERR_UNSUPPORTED;   // O is already float32
+    return cuda_status(launch_fwd_simt((const float*)q, (const float*)k, (const float*)v, (float*)o, sd, a, st));
+  }
+  CUtensorMap mq, mk, mv, mo;
+  if ((s = map16(&mq, q, p, sd)) != FA_OK || (s = map16(&mk, k, p, sd)) != FA_OK ||
+      (s = map16(&mv, v, p, sd)) != FA_OK || (s = map16(&mo, o, p, sd)) != FA_OK)
+    return s;
+  return cuda_status(launch_fwd_tc(p->dtype, fwd_p_in_tmem(), mq, mk, mv, mo, a, st));
+}
+
+fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+  fa_status s = check_params(p);
+  if (s != FA_OK) return s;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  const Layout L = layout(p, true);
+  if (ws == nullptr || ws_bytes < L.total || !aligned16(ws)) return FA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const Strides sd = strides_of(p);
+
+  BwdArgs a{};
+  a.B = p->B; a.H = p->H; a.N = p->N;
+  a.nq = L.nq;
+  a.npad = L.npad;
+  a.scale = scale_of(p);
+  a.scale_log2 = a.scale * 1.4426950408889634f;
+  a.mask = mask_of(p, L, w);
+  a.drop = dropout_of(p);
+  a.lse2 = reinterpret_cast<const float*>(w + L.lse2);
+  a.dvec = reinterpret_cast<const float*>(w + L.dvec);
+  a.status = reinterpret_cast<int*>(w + L.status);
+
+  if ((s = prepare_common(p, L, w, st)) != FA_OK) return s;
+  float* dqacc = p->dtype == FA_DT_F32 ? nullptr : reinterpret_cast<float*>(w + L.dqacc);
+  cudaError_t e = launch_bwd_prep(p->dtype, o, dout, sd, lse, p->B, p->H, p->N, L.npad,
+                                  reinterpret_cast<float*>(w + L.lse2), reinterpret_cast<float*>(w + L.dvec), dqacc,
+                                  st);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if (p->dtype == FA_DT_F32)
+    return cuda_status(launch_bwd_simt((const float*)q, (const float*)k, (const float*)v, (const float*)dout,
+                                       (float*)dq, (float*)dk, (float*)dv, sd, a, st));
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv, macc;
+  Strides acc_st{(int64_t)p->H * p->N * kHeadDim, (int64_t)p->N * kHeadDim, kHeadDim};
+  if ((s = map16(&mq, q, p, sd)) != FA_OK || (s = map16(&mk, k, p, sd)) != FA_OK ||
+      (s = map16(&mv, v, p, sd)) != FA_OK || (s = map16(&mdo, dout, p, sd)) != FA_OK ||
+      (s = map16(&mdk, dk, p, sd)) != FA_OK || (s = map16(&mdv, dv, p, sd)) != FA_OK ||
+      (s = make_map(&macc, dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kHeadDim, 32, p, acc_st)) != FA_OK)
+    return s;
+  if ((e = launch_bwd_tc(p->dtype, mq, mk, mv, mdo, mdk, mdv, macc, a, st)) != cudaSuccess) return FA_ERR_CUDA;
+  return cuda_status(launch_dq_convert(p->dtype, dqacc, dq, sd, p->B, p->H, p->N, st));
+}
+
+fa_status fa_check_status(const void* ws, void* stream) {
+  if (ws == nullptr) return FA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  return v == 0 ? FA_OK : (fa_status)v;
+}
+
+fa_status fa_dropout_mask(const fa_params* p, int32_t b, int32_t h, int32_t row0, int32_t nrows, uint8_t* out,
+                          void* stream) {
+  if (p == nullptr || out == nullptr) return FA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->N < 1) return FA_ERR_INVALID_ARG;
+  if (!(p->dropout_p >= 0.f && p->dropout_p < 1.f)) return FA_ERR_INVALID_ARG;
+  if (b < 0 || b >= p->B || h < 0 || h >= p->H || row0 < 0 || nrows < 0 || row0 + (int64_t)nrows > p->N)
+    return FA_ERR_INVALID_ARG;
+  if ((long long)p->B * p->H * p->N >= (1ll << 32)) return FA_ERR_UNSUPPORTED;
+  return cuda_status(launch_dropout_mask(dropout_of(p), p->H, p->N, b, h, row0, nrows, out,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+int32_t fa_version(void) { return 100; }
+
+}  // extern "C"

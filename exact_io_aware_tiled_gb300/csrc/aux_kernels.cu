@@ -1,0 +1,173 @@
+// aux_kernels.cu -- small HBM-bound kernels around the attention kernels.
+//
+//   * bwd_prep: D_i = dO_i . O_i (tonho.wtf, "como funciona": the softmax
+//     gradient's row term is a length-d dot product instead of a length-N
+//     reduction), the logsumexp rescaled to log2 units, both written to
+//     128-row-padded arrays the backward kernel bulk-copies per tile;
+//   * dq_convert: float32 dQ accumulator -> storage dtype;
+//   * block_lists: row / column index lists of a block-sparse mask
+//     (agihunt.info, block-sparse paragraph: only nonzero blocks are visited);
+//   * dropout_mask: the keep-mask of the Philox mapping, for tests.
+#include "common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <typename T> __device__ __forceinline__ float ldf(const T* p) { return Cvt<T>::to_f(*p); }
+template <> __device__ __forceinline__ float ldf<float>(const float* p) { return *p; }
+
+// One warp per query row; lanes cover 2 of the 64 columns each.
+template <typename T>
+__global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ dout, Strides st,
+                                const float* __restrict__ lse, int B, int H, int N, int npad,
+                                float* __restrict__ lse2, float* __restrict__ dvec) {
+  const int warps = blockDim.x >> 5;
+  const long long row = (long long)blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long long total = (long long)B * H * npad;
+  if (row >= total) return;
+  const int bh = (int)(row / npad);
+  const int i = (int)(row % npad);
+  float d = 0.f;
+  if (i < N) {
+    const int b = bh / H, h = bh % H;
+    const size_t off = (size_t)b * st.b + (size_t)h * st.h + (size_t)i * st.n;
+    d = ldf(o + off + lane) * ldf(dout + off + lane) + ldf(o + off + lane + 32) * ldf(dout + off + lane + 32);
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) d += __shfl_xor_sync(0xffffffffu, d, s);
+  if (lane == 0) {
+    float l2 = INFINITY;
+    if (i < N) {
+      const float v = lse[(size_t)bh * N + i];
+      l2 = (v == -INFINITY) ? INFINITY : v * kLog2e;
+    }
+    lse2[row] = l2;
+    dvec[row] = i < N ? d : 0.f;
+  }
+}
+
+template <typename T>
+__global__ void dq_convert_kernel(const float* __restrict__ acc, T* __restrict__ dq, Strides st, int H, int N,
+                                  long long nrows) {
+  // 8 consecutive elements per thread
+  const long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (e >= nrows * 64) return;
+  const long long row = e / 64;
+  const int c = (int)(e % 64);
+  const int bh = (int)(row / N), i = (int)(row % N);
+  const int b = bh / H, h = bh % H;
+  const float4 x0 = *reinterpret_cast<const float4*>(acc + e);
+  const float4 x1 = *reinterpret_cast<const float4*>(acc + e + 4);
+  uint4 w;
+  w.x = Cvt<T>::pack(x0.x, x0.y);
+  w.y = Cvt<T>::pack(x0.z, x0.w);
+  w.z = Cvt<T>::pack(x1.x, x1.y);
+  w.w = Cvt<T>::pack(x1.z, x1.w);
+  *reinterpret_cast<uint4*>(dq + (size_t)b * st.b + (size_t)h * st.h + (size_t)i * st.n + c) = w;
+}
+
+// blockIdx.y == 0: row lists (kept kv tiles of q tile blockIdx.x);
+// blockIdx.y == 1: column lists (q tiles keeping kv tile blockIdx.x).
+__global__ void block_lists_kernel(const uint8_t* __restrict__ mask, int nb, int16_t* __restrict__ row_list,
+                                   int32_t* __restrict__ row_cnt, int16_t* __restrict__ col_list,
+                                   int32_t* __restrict__ col_cnt) {
+  const int t = blockIdx.x;
+  const bool rows = blockIdx.y == 0;
+  int16_t* out = (rows ? row_list : col_list) + (size_t)t * nb;
+  __shared__ int base;
+  if (threadIdx.x == 0) base = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  for (int s0 = 0; s0 < nb; s0 += blockDim.x) {
+    const int s = s0 + threadIdx.x;
+    const bool keep = s < nb && (rows ? mask[(size_t)t * nb + s] : mask[(size_t)s * nb + t]) != 0;
+    // ordered compaction: warp ballot, then warps in order
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    __shared__ int wcount[32];
+    if (lane == 0) wcount[threadIdx.x >> 5] = __popc(bal);
+    __syncthreads();
+    int before = base;
+    for (int w = 0; w < (int)(threadIdx.x >> 5); ++w) before += wcount[w];
+    if (keep) out[before + __popc(bal & ((1u << lane) - 1u))] = (int16_t)s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += wcount[w];
+      base += tot;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) (rows ? row_cnt : col_cnt)[t] = base;
+}
+
+__global__ void dropout_mask_kernel(DropoutArgs d, int H, int N, int b, int h, int row0, int nrows,
+                                    uint8_t* __restrict__ out) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // one 8-key group
+  const int groups = (N + 7) / 8;
+  if (e >= (long long)nrows * groups) return;
+  const int r = (int)(e / groups), g = (int)(e % groups);
+  const uint32_t row_g = (uint32_t)(b * H + h) * (uint32_t)N + (uint32_t)(row0 + r);
+  const uint32_t bits = dropout_keep8((uint32_t)g, row_g, d);
+  for (int t = 0; t < 8; ++t) {
+    const int j = g * 8 + t;
+    if (j < N) out[(size_t)r * N + j] = (uint8_t)((bits >> t) & 1u);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(int dtype, const void* o, const void* dout, Strides st, const float* lse, int B, int H,
+                            int N, int npad, float* lse2, float* dvec, float* dqacc, cudaStream_t s) {
+  const long long rows = (long long)B * H * npad;
+  const int threads = 256;
+  const long long blocks = (rows + (threads / 32) - 1) / (threads / 32);
+  if (dtype == FA_DT_BF16)
+    bwd_prep_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, s>>>(
+        (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, st, lse, B, H, N, npad, lse2, dvec);
+  else if (dtype == FA_DT_F16)
+    bwd_prep_kernel<__half><<<(unsigned)blocks, threads, 0, s>>>((const __half*)o, (const __half*)dout, st, lse, B,
+                                                                 H, N, npad, lse2, dvec);
+  else
+    bwd_prep_kernel<float><<<(unsigned)blocks, threads, 0, s>>>((const float*)o, (const float*)dout, st, lse, B, H,
+                                                                N, npad, lse2, dvec);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (dqacc != nullptr) e = cudaMemsetAsync(dqacc, 0, (size_t)B * H * N * 64 * sizeof(float), s);
+  return e;
+}
+
+cudaError_t launch_dq_convert(int dtype, const float* dqacc, void* dq, Strides st, int B, int H, int N,
+                              cudaStream_t s) {
+  const long long nrows = (long long)B * H * N;
+  const long long threads_total = nrows * 8;
+  const int threads = 256;
+  const unsigned blocks = (unsigned)((threads_total + threads - 1) / threads);
+  if (blocks == 0) return cudaSuccess;
+  if (dtype == FA_DT_BF16)
+    dq_convert_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(dqacc, (__nv_bfloat16*)dq, st, H, N, nrows);
+  else
+    dq_convert_kernel<__half><<<blocks, threads, 0, s>>>(dqacc, (__half*)dq, st, H, N, nrows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_block_lists(const uint8_t* mask, int nb, int16_t* row_list, int32_t* row_cnt, int16_t* col_list,
+                               int32_t* col_cnt, cudaStream_t s) {
+  dim3 grid(nb, 2);
+  block_lists_kernel<<<grid, 256, 0, s>>>(mask, nb, row_list, row_cnt, col_list, col_cnt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dropout_mask(const DropoutArgs& d, int H, int N, int b, int h, int row0, int nrows, uint8_t* out,
+                                cudaStream_t s) {
+  const long long groups = (long long)nrows * ((N + 7) / 8);
+  if (groups == 0) return cudaSuccess;
+  const int threads = 256;
+  dropout_mask_kernel<<<(unsigned)((groups + threads - 1) / threads), threads, 0, s>>>(d, H, N, b, h, row0, nrows,
+                                                                                         out);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

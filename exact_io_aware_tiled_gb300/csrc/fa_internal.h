@@ -1,0 +1,91 @@
+// fa_internal.h -- definitions shared by the host library and the kernels.
+#pragma once
+#include <cstdint>
+#include <cstddef>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// A bounded device-side wait gives up after this many nanoseconds.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+constexpr int kTile = 128;       // query rows (and key rows) per tile
+constexpr int kHeadDim = 64;     // head dimension handled by the kernels
+
+struct DropoutArgs {
+  uint32_t k0, k1;         // Philox key = (lo32(seed), hi32(seed))
+  uint32_t off_lo, off_hi; // counter words 2, 3
+  uint32_t threshold;      // keep iff 16-bit slice >= threshold
+  float rp;                // 1 / (1 - p)
+  int enabled;
+};
+
+struct MaskArgs {
+  int causal;
+  const int32_t* seqlens_k;   // device [B] or nullptr
+  const int16_t* row_list;    // [nb][nb]: kept kv tiles of each q tile, ascending
+  const int32_t* row_cnt;     // [nb]
+  const int16_t* col_list;    // [nb][nb]: q tiles that keep each kv tile, ascending
+  const int32_t* col_cnt;     // [nb]
+  int nb;                     // tiles per side (0 when dense)
+};
+
+struct FwdArgs {
+  int B, H, N;
+  int nq;                     // ceil(N / 128)
+  int npairs;                 // ceil(nq / 2)
+  float scale_log2;           // tau * log2(e)
+  MaskArgs mask;
+  DropoutArgs drop;
+  float* lse;                 // [B,H,N]
+  float* o_f32;               // optional [B,H,N,64]
+  int* status;
+};
+
+struct BwdArgs {
+  int B, H, N;
+  int nq;                     // ceil(N / 128)
+  int npad;                   // nq * 128
+  float scale;                // tau
+  float scale_log2;           // tau * log2(e)
+  MaskArgs mask;
+  DropoutArgs drop;
+  const float* lse2;          // [B*H][npad]: LSE*log2(e), +inf for rows without keys / padding
+  const float* dvec;          // [B*H][npad]: D = rowsum(dO o O), 0 on padding
+  int* status;
+};
+
+// ---------------------------------------------------------------------------
+// Launchers (defined in the .cu files; all enqueue on `stream`).
+// ---------------------------------------------------------------------------
+cudaError_t launch_fwd_tc(int dtype, bool p_in_tmem, const CUtensorMap& q, const CUtensorMap& k,
+                          const CUtensorMap& v, const CUtensorMap& o, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
+                          const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s);
+
+struct Strides { int64_t b, h, n; };
+
+cudaError_t launch_fwd_simt(const float* q, const float* k, const float* v, float* o, Strides st,
+                            const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_simt(const float* q, const float* k, const float* v, const float* dout,
+                            float* dq, float* dk, float* dv, Strides st, const BwdArgs& a,
+                            cudaStream_t s);
+
+// D = rowsum(dO o O) and the padded LSE*log2e / D arrays; zeroes dqacc if given.
+cudaError_t launch_bwd_prep(int dtype, const void* o, const void* dout, Strides st, const float* lse,
+                            int B, int H, int N, int npad, float* lse2, float* dvec, float* dqacc,
+                            cudaStream_t s);
+// dq = dqacc (already scaled) cast to dtype with strides.
+cudaError_t launch_dq_convert(int dtype, const float* dqacc, void* dq, Strides st, int B, int H, int N,
+                              cudaStream_t s);
+// Row / column block lists of a dense [nb][nb] uint8 block mask.
+cudaError_t launch_block_lists(const uint8_t* mask, int nb, int16_t* row_list, int32_t* row_cnt,
+                               int16_t* col_list, int32_t* col_cnt, cudaStream_t s);
+cudaError_t launch_dropout_mask(const DropoutArgs& d, int H, int N, int b, int h, int row0, int nrows,
+                                uint8_t* out, cudaStream_t s);
+
+}  // namespace fa

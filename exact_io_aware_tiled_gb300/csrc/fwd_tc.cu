@@ -1,0 +1,445 @@
+// fwd_tc.cu -- forward attention kernel for 16-bit inputs on sm_103a.
+//
+// Method (the pages): Q-outer tiling with the online-softmax recurrence and
+// deferred normalisation (lynx-cortex "FlashAttention como una optimizacion
+// de roofline", section "El algoritmo Flash (forward)"; marketmaker.cc,
+// "O algoritmo de atencao do Flash"), causal / padded / sparse tiles skipped
+// (marketmaker.cc, "O mascaramento causal"; agihunt.info, block-sparse
+// paragraph), mask and dropout applied to the score tile on chip
+// (agihunt.info, fused-kernel paragraph).  Only O and the per-row
+// logsumexp leave the chip.
+//
+// GB300 mapping (ours, not the pages'):
+//   * one CTA = two 128-row query tiles ("slots") of one (b, h) head;
+//   * warp 8 (one thread) streams K/V tiles with TMA into a ring of NS
+//     stages; a stage is shared by both slots when both need the same KV tile
+//     at the same step;
+//   * warp 9 (one thread) issues tcgen05 MMAs: S_x = Q_x K^T into tensor
+//     memory, then O_x += P_x V with P_x read from tensor memory (or, in the
+//     alternative build, from shared memory);
+//   * warps 0-3 / 4-7 run the softmax of slot 0 / 1, one thread per query
+//     row (= tensor-memory lane): max, exp2, row sums, dropout, P in 16 bit;
+//   * O is rescaled only when the running row max grows by more than 2^8
+//     (the final O / l and the logsumexp use the same reference max, so the
+//     result is unchanged); O is normalised by the sum of the rounded P that
+//     the MMA actually consumed;
+//   * epilogue: O / l -> 16 bit -> shared memory (128-B swizzle) -> TMA store,
+//     which clips rows >= N; the logsumexp goes out with plain stores.
+// Tensor memory per slot: S 128 columns | P 64 | O 64  (512 in total).
+#include "common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <bool kPTmem> struct FwdCfg {
+  static constexpr int NS = kPTmem ? 5 : 3;              // K/V stages
+  static constexpr int kQ = 0;                           // 2 x 16 KB
+  static constexpr int kK = 32768;                       // NS x 16 KB
+  static constexpr int kV = kK + NS * 16384;             // NS x 16 KB
+  static constexpr int kP = kV + NS * 16384;             // 2 x 32 KB (shared-memory P only)
+  static constexpr int kBar = kP + (kPTmem ? 0 : 65536);
+  static constexpr int kBytes = kBar + 256;
+  static constexpr int kDyn = kBytes + 1024;             // + alignment slack
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t mma_done;
+  uint64_t k_full[5], v_full[5], kv_empty[5];
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Slot {
+  int qt;                 // query tile index
+  int n;                  // kv steps
+  const int16_t* list;    // sparse kv list or nullptr
+  __device__ __forceinline__ int kv(int s) const { return list ? (int)list[s] : s; }
+};
+
+__device__ __forceinline__ Slot make_slot(const FwdArgs& a, int qt, int Lk) {
+  Slot sl;
+  sl.qt = qt;
+  sl.list = nullptr;
+  sl.n = 0;
+  if (qt >= a.nq) return sl;
+  int lim = (Lk + kTile - 1) / kTile;
+  if (a.mask.causal) lim = min(lim, qt + 1);
+  if (a.mask.row_list != nullptr) {
+    sl.list = a.mask.row_list + (size_t)qt * a.mask.nb;
+    const int cnt = a.mask.row_cnt[qt];
+    int n = 0;
+    while (n < cnt && sl.list[n] < lim) ++n;
+    sl.n = n;
+  } else {
+    sl.n = lim;
+  }
+  return sl;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
+  const bool ok = mbar_wait(bar, parity, ctl);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <typename T, bool kPTmem>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+              const FwdArgs a) {
+  using C = FwdCfg<kPTmem>;
+  constexpr int NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kBar);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work item: (b, h, pair of query tiles); heaviest pairs launch first
+  const int BH = a.B * a.H;
+  const int pair = a.npairs - 1 - (int)(blockIdx.x / BH);
+  const int bh = (int)(blockIdx.x % BH);
+  const int b = bh / a.H, h = bh % a.H;
+  int Lk = a.N;
+  if (a.mask.seqlens_k != nullptr) Lk = max(0, min(a.N, a.mask.seqlens_k[b]));
+  Slot sl[2];
+  sl[0] = make_slot(a, 2 * pair, Lk);
+  sl[1] = make_slot(a, 2 * pair + 1, Lk);
+  const int smax = max(sl[0].n, sl[1].n);
+
+  WaitCtl ctl{a.status, &bars->abort};
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars->s_full[x], 1);
+      mbar_init(&bars->p_full[x], 128);
+      mbar_init(&bars->o_full[x], 1);
+    }
+    mbar_init(&bars->mma_done, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 8) {
+    // ===================== TMA producer =====================
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      const uint32_t qbytes = (sl[0].n > 0 ? 16384u : 0u) + (sl[1].n > 0 ? 16384u : 0u);
+      if (qbytes > 0) {
+        mbar_expect_tx(&bars->q_full, qbytes);
+        for (int x = 0; x < 2; ++x)
+          if (sl[x].n > 0) tma_load_4d(smem + C::kQ + x * 16384, &tmQ, &bars->q_full, 0, sl[x].qt * kTile, h, b);
+      }
+      int ld = 0;
+      bool ok = true;
+      for (int s = 0; s < smax && ok; ++s) {
+        const int kvA = s < sl[0].n ? sl[0].kv(s) : -1;
+        const int kvB = s < sl[1].n ? sl[1].kv(s) : -1;
+        int todo[2] = {kvA, (kvB >= 0 && kvB != kvA) ? kvB : -1};
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (todo[t] < 0) continue;
+          const int st = ld % NS;
+          const uint32_t ph = (uint32_t)(ld / NS) & 1u;
+          ++ld;
+          if (!mbar_wait(&bars->kv_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+          mbar_expect_tx(&bars->k_full[st], 16384);
+          tma_load_4d(smem + C::kK + st * 16384, &tmK, &bars->k_full[st], 0, todo[t] * kTile, h, b);
+          mbar_expect_tx(&bars->v_full[st], 16384);
+          tma_load_4d(smem + C::kV + st * 16384, &tmV, &bars->v_full[st], 0, todo[t] * kTile, h, b);
+        }
+      }
+      // Before leaving, make sure no load is still writing shared memory.
+      for (int j = max(0, ld - NS); j < ld; ++j) {
+        mbar_wait(&bars->k_full[j % NS], (uint32_t)(j / NS) & 1u, ctl);
+        mbar_wait(&bars->v_full[j % NS], (uint32_t)(j / NS) & 1u, ctl);
+      }
+      if (qbytes > 0) mbar_wait(&bars->q_full, 0, ctl);
+    }
+  } else if (warp == 9) {
+    // ===================== MMA issuer =====================
+    if (lane == 0 && smax > 0) {
+      constexpr int ab = Cvt<T>::kAB;
+      constexpr uint32_t idS = idesc_f16(128, 128, ab, 0, 0);
+      constexpr uint32_t idPV = idesc_f16(128, 64, ab, 0, 1);
+      const uint32_t sQ = smem_u32(smem + C::kQ), sK = smem_u32(smem + C::kK), sV = smem_u32(smem + C::kV);
+      const uint32_t sP = smem_u32(smem + C::kP);
+      bool ok = mbar_wait(&bars->q_full, 0, ctl);
+      int ld = 0;
+      int pst[2] = {-1, -1};
+      uint32_t pph[2] = {0, 0};
+      bool pshared = false;   // both slots used one stage at the previous step
+      for (int s = 0; s <= smax && ok; ++s) {
+        int st[2] = {-1, -1};
+        uint32_t ph[2] = {0, 0};
+        bool shared = false;
+        if (s < smax) {
+          const int kvA = s < sl[0].n ? sl[0].kv(s) : -1;
+          const int kvB = s < sl[1].n ? sl[1].kv(s) : -1;
+          if (kvA >= 0) { st[0] = ld % NS; ph[0] = (uint32_t)(ld / NS) & 1u; ++ld; }
+          if (kvB >= 0) {
+            if (kvB == kvA) { st[1] = st[0]; ph[1] = ph[0]; shared = true; }
+            else { st[1] = ld % NS; ph[1] = (uint32_t)(ld / NS) & 1u; ++ld; }
+          }
+        }
+        for (int x = 0; x < 2 && ok; ++x) {
+          const int n = sl[x].n;
+          if (n == 0 || s > n) continue;
+          const uint32_t tS = tmem + x * 256, tP = tS + 128, tO = tS + 192;
+          if (s > 0) {
+            // O_x += P_x(s-1) V(s-1)
+            ok = mbar_wait(&bars->p_full[x], (uint32_t)(s - 1) & 1u, ctl) &&
+                 mbar_wait(&bars->v_full[pst[x]], pph[x], ctl);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t vb = sV + pst[x] * 16384;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t bd = sdesc_sw128(vb + k * 2048, 16384, 1024);
+              const uint32_t acc = (s > 1 || k > 0) ? 1u : 0u;
+              if constexpr (kPTmem) {
+                mma_ts(tO, tP + k * 8, bd, idPV, acc);
+              } else {
+                const uint64_t adsc = sdesc_sw128(sP + x * 32768 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+                mma_ss(tO, adsc, bd, idPV, acc);
+              }
+            }
+            // A stage both slots read is released after slot 1's PV.
+            if (!(pshared && x == 0)) mma_commit(&bars->kv_empty[pst[x]]);
+            if (s == n) mma_commit(&bars->o_full[x]);
+          }
+          if (s < n) {
+            // S_x(s) = Q_x K(s)^T
+            if (!(ok = mbar_wait(&bars->k_full[st[x]], ph[x], ctl))) break;
+            tc_fence_after();
+            const uint32_t qb = sQ + x * 16384, kb = sK + st[x] * 16384;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tS, sdesc_sw128(qb + k * 32, 16, 1024), sdesc_sw128(kb + k * 32, 16, 1024), idS,
+                     k > 0 ? 1u : 0u);
+            mma_commit(&bars->s_full[x]);
+          }
+        }
+        pst[0] = st[0]; pst[1] = st[1];
+        pph[0] = ph[0]; pph[1] = ph[1];
+        pshared = shared;
+      }
+      // All MMAs must have retired before tensor memory is released.
+      mma_commit(&bars->mma_done);
+      mbar_wait(&bars->mma_done, 0, ctl);
+    }
+  } else {
+    // ===================== softmax warps =====================
+    const int x = warp >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;          // row within the tile = TMEM lane
+    const Slot& S = sl[x];
+    const int i = S.qt * kTile + r;             // global query row
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + x * 256 + lane_off, tP = tS + 128, tO = tS + 192;
+    const float sl2 = a.scale_log2;
+    const int jmax = a.mask.causal ? min(Lk - 1, i) : (Lk - 1);
+    const uint32_t row_g = (uint32_t)(b * a.H + h) * (uint32_t)a.N + (uint32_t)i;
+
+    float m_run = -INFINITY;
+    float l_true = 0.f, l_rnd = 0.f;
+    bool ok = true;
+    for (int s = 0; s < S.n; ++s) {
+      const int kv = S.kv(s);
+      if (!(ok = warp_wait(&bars->s_full[x], (uint32_t)s & 1u, ctl))) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+      tmem_wait_ld();
+
+      // mask (only boundary tiles) and row max of the raw scores
+      const int jl = jmax - kv * kTile;
+      float mx = -INFINITY;
+      if (jl >= kTile - 1) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          if (c > jl) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
+        }
+      }
+      mx *= sl2;
+      // running reference max: moved only when the tile max exceeds it by 2^8
+      float m_new = m_run;
+      if (mx > m_run + kRescaleThreshold) m_new = mx;
+      const bool rescale = (m_new != m_run) && (m_run != -INFINITY) && (s > 0);
+      const float alpha = (m_new != m_run && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
+      m_run = m_new;
+      l_true *= alpha;
+      l_rnd *= alpha;
+      const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+
+      uint32_t keep[4] = {~0u, ~0u, ~0u, ~0u};
+      if (a.drop.enabled) {
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {
+          const uint32_t bits = dropout_keep8((uint32_t)(kv * 16 + g), row_g, a.drop);
+          keep[g >> 2] = (g & 3) == 0 ? bits : (keep[g >> 2] | (bits << ((g & 3) * 8)));
+        }
+      }
+      // P = exp2(S * tau*log2e - m) in two halves of 64 keys (32 packed words)
+      float lt0 = 0.f, lt1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c2 = 0; c2 < 64; c2 += 2) {
+          const int c = hf * 64 + c2;
+          const float p0 = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -mref));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2, -mref));
+          lt0 += p0;
+          lt1 += p1;
+          uint32_t u = Cvt<T>::pack(p0, p1);
+          lr0 += Cvt<T>::lo(u);
+          lr1 += Cvt<T>::hi(u);
+          if (a.drop.enabled) {
+            const bool k0 = (keep[c >> 5] >> (c & 31)) & 1u;
+            const bool k1 = (keep[c >> 5] >> ((c + 1) & 31)) & 1u;
+            u = Cvt<T>::pack(k0 ? p0 * a.drop.rp : 0.f, k1 ? p1 * a.drop.rp : 0.f);
+          }
+          pk[c2 >> 1] = u;
+        }
+        if constexpr (kPTmem) {
+          tmem_st32(tP + hf * 32, pk);
+        } else {
+          uint8_t* pb = smem + C::kP + x * 32768 + hf * 16384;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t off = r * 128 + (((j ^ r) & 7) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         :: "r"(smem_u32(pb + off)), "r"(pk[j * 4]), "r"(pk[j * 4 + 1]), "r"(pk[j * 4 + 2]),
+                            "r"(pk[j * 4 + 3]) : "memory");
+          }
+        }
+      }
+      l_true += lt0 + lt1;
+      l_rnd += lr0 + lr1;
+
+      if (rescale) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t o[32];
+          tmem_ld32(tO + hf * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st32(tO + hf * 32, o);
+        }
+      }
+      if (kPTmem || rescale) tmem_wait_st();
+      if constexpr (!kPTmem) fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[x]);
+    }
+
+    // ---- epilogue: O / l -> 16 bit -> shared -> TMA store; logsumexp
+    named_bar_sync(1 + x, 128);
+    if (!bars->abort) {
+      float o[64];
+      if (S.n > 0) {
+        if (warp_wait(&bars->o_full[x], 0, ctl)) {
+          tc_fence_after();
+          uint32_t raw[2][32];
+          tmem_ld32(tO, raw[0]);
+          tmem_ld32(tO + 32, raw[1]);
+          tmem_wait_ld();
+          const float inv = l_rnd > 0.f ? 1.f / l_rnd : 0.f;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) o[c] = __uint_as_float(raw[c >> 5][c & 31]) * inv;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) o[c] = 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) o[c] = 0.f;
+      }
+      uint8_t* ob = smem + C::kQ + x * 16384;   // Q_x is dead once O_x is final
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t w[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) w[t] = Cvt<T>::pack(o[j * 8 + 2 * t], o[j * 8 + 2 * t + 1]);
+        const uint32_t off = r * 128 + (((j ^ r) & 7) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(smem_u32(ob + off)), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + x, 128);
+      if (r == 0 && S.qt < a.nq) {
+        tma_store_4d(&tmO, ob, 0, S.qt * kTile, h, b);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+      if (i < a.N && S.qt < a.nq) {
+        const size_t row = (size_t)(b * a.H + h) * a.N + i;
+        a.lse[row] = l_true > 0.f ? (m_run + lg2(l_true)) * kLn2 : -INFINITY;
+        if (a.o_f32 != nullptr) {
+          float4* dst = reinterpret_cast<float4*>(a.o_f32 + row * 64);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) dst[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <typename T, bool kPTmem>
+cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                     const FwdArgs& a, cudaStream_t s) {
+  using C = FwdCfg<kPTmem>;
+  auto kern = fwd_tc_kernel<T, kPTmem>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDyn);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(a.npairs * a.B * a.H);
+  if (grid == 0) return cudaSuccess;
+  kern<<<grid, kThreads, C::kDyn, s>>>(q, k, v, o, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(int dtype, bool p_in_tmem, const CUtensorMap& q, const CUtensorMap& k,
+                          const CUtensorMap& v, const CUtensorMap& o, const FwdArgs& a, cudaStream_t s) {
+  if (dtype == FA_DT_BF16)
+    return p_in_tmem ? launch_t<__nv_bfloat16, true>(q, k, v, o, a, s) : launch_t<__nv_bfloat16, false>(q, k, v, o, a, s);
+  return p_in_tmem ? launch_t<__half, true>(q, k, v, o, a, s) : launch_t<__half, false>(q, k, v, o, a, s);
+}
+
+}  // namespace fa

@@ -1,0 +1,161 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact, IO-aware, tiled attention library.
+ *
+ * The library computes exact scaled-dot-product attention
+ *     O = softmax(tau * Q K^T + mask) V
+ * tile by tile with the online-softmax recurrence (running row max m, running
+ * row sum l, accumulator rescaled by exp(m_old - m_new)), never writes the
+ * N x N score or probability matrix to memory, and saves only O and the per-row
+ * logsumexp.  The backward pass recomputes the probability tiles on chip from
+ * Q, K, V and the logsumexp.  Sources of the method:
+ *   - "FlashAttention: Fast and Memory-Efficient Exact Attention with
+ *     IO-Awareness" (Dao et al., 2022), as summarised on tonho.wtf (section
+ *     "como funciona": the recurrence, the saved statistics, recomputation in
+ *     the backward pass and D_i = dO_i . O_i) and agihunt.info (the fused
+ *     forward/backward kernels, on-chip masking and dropout replay, and the
+ *     block-sparse variant);
+ *   - marketmaker.cc "Flash Attention" post (Q-outer loop, causal tile
+ *     skipping, the PyTorch (batch, heads, seq, head_dim) interface);
+ *   - lynx-cortex "FlashAttention como una optimizacion de roofline" (the
+ *     Q-outer loop with deferred normalisation used by the forward kernel).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors Q, K, V, O, dO, dQ, dK, dV are logical [B, H, N, d] arrays of
+ *     one dtype, addressed as base + b*stride_b + h*stride_h + n*stride_n + c
+ *     (element strides; the head dimension is contiguous).  LSE is a
+ *     contiguous float32 [B, H, N] array.
+ *   - Ownership: the caller owns every buffer and the stream.  The library
+ *     never allocates, frees or synchronises device memory, except that
+ *     fa_check_status synchronises the stream it is given.  Work is enqueued
+ *     asynchronously on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  All pointers named "device" must be device-accessible.
+ *   - Errors found on the host (shapes, alignment, unsupported combinations,
+ *     too small a workspace, a failed launch) are returned synchronously and
+ *     nothing is enqueued.  There is no silent fallback to another algorithm:
+ *     every unsupported combination returns FA_ERR_UNSUPPORTED.
+ *   - Device-side waits are bounded; a wait that runs out records
+ *     FA_ERR_TIMEOUT in the workspace status word, the kernel releases its
+ *     resources and exits, and fa_check_status reports it.
+ *   - Re-entrant: no global mutable state.  Concurrent calls need separate
+ *     workspaces.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, bad probability ...   */
+  FA_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement    */
+  FA_ERR_MISALIGNED = 3,    /* base pointer or stride breaks the 16-B rule    */
+  FA_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than the query says  */
+  FA_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed              */
+  FA_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out             */
+} fa_status;
+
+typedef enum { FA_DT_F32 = 0, FA_DT_F16 = 1, FA_DT_BF16 = 2 } fa_dtype;
+
+typedef struct {
+  int32_t B, H, N, d;        /* batch, heads, sequence length, head dim (64)    */
+  int32_t dtype;             /* fa_dtype of Q,K,V,O,dO,dQ,dK,dV                 */
+  int64_t stride_b;          /* element strides shared by all [B,H,N,d] tensors */
+  int64_t stride_h;
+  int64_t stride_n;
+  float scale;               /* tau; <= 0 selects 1/sqrt(d)                     */
+  int32_t causal;            /* nonzero: key j visible to query i iff j <= i    */
+  const int32_t *seqlens_k;  /* device [B] or NULL: keys j >= L_b are masked     */
+  float dropout_p;           /* in [0, 1); 0 disables dropout                   */
+  uint64_t seed;             /* Philox4x32-10 key = (lo32(seed), hi32(seed))    */
+  uint64_t offset;           /* Philox counter words 2,3 = (lo32, hi32)(offset) */
+  const uint8_t *block_mask; /* device [nb][nb] (nb = ceil(N/block_size)),
+                                nonzero = keep the block; or NULL (dense)       */
+  int32_t block_size;        /* must be 128 when block_mask != NULL             */
+  float *o_f32;              /* optional device [B,H,N,d] contiguous float32:
+                                fa_fwd also writes O before its final rounding
+                                to the storage dtype (parity diagnostics)       */
+} fa_params;
+
+/* ---------------------------------------------------------------------------
+ * fa_fwd_workspace_size / fa_bwd_workspace_size
+ * Bytes of device workspace fa_fwd / fa_bwd need for `p` (0 is never
+ * returned: the status word is always present).  Pure host function.
+ * The backward workspace holds the float32 dQ accumulator [B,H,N,d] (16-bit
+ * dtypes), D = rowsum(dO o O) [B,H,N], block lists and the status word.
+ * ------------------------------------------------------------------------- */
+size_t fa_fwd_workspace_size(const fa_params *p);
+size_t fa_bwd_workspace_size(const fa_params *p);
+
+/* ---------------------------------------------------------------------------
+ * fa_fwd -- forward pass.
+ * Computes, for every (b, h) head, O = P~ V with P = softmax(tau Q K^T) over
+ * the visible keys (causal AND key-padding AND block mask), P~ = Z o P/(1-p)
+ * when dropout is on, and LSE_i = m_i + ln l_i (natural log, tau-scaled
+ * scores; -inf for a row with no visible key, whose O row is 0).
+ * Method: Q-outer tiling with the online-softmax recurrence and deferred
+ * normalisation (lynx-cortex, "El algoritmo Flash (forward)"; marketmaker.cc,
+ * "O algoritmo de atencao do Flash"), whole future / masked / sparse tiles
+ * skipped (marketmaker.cc, "O mascaramento causal"; agihunt.info, block-sparse
+ * paragraph), dropout applied on chip (agihunt.info, fused-kernel paragraph).
+ *   q, k, v : device [B,H,N,d] inputs (strides in p)
+ *   o       : device [B,H,N,d] output, same dtype and strides
+ *   lse     : device float32 [B,H,N] output
+ *   ws      : device workspace of ws_bytes >= fa_fwd_workspace_size(p)
+ * Dropout element (b,h,i,j) is kept iff the 16-bit slice (j & 7) of
+ * Philox4x32-10(counter = (j>>3, (b*H+h)*N+i, lo32(offset), hi32(offset)),
+ * key = (lo32(seed), hi32(seed))) is >= round(p * 65536); slice t is half
+ * (t & 1) of output word (t >> 1), low half first.  Requires B*H*N < 2^32.
+ * ------------------------------------------------------------------------- */
+fa_status fa_fwd(const fa_params *p, const void *q, const void *k, const void *v,
+                 void *o, float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * fa_bwd -- backward pass by recomputation (tonho.wtf, "como funciona": only
+ * O, the softmax statistics and the RNG state are kept; S and P are rebuilt
+ * on chip; D_i = dO_i . O_i replaces a length-N reduction).
+ * For upstream gradient dO it computes, with the same mask and dropout
+ * replay as fa_fwd:
+ *   dV = P~^T dO;  dP = Z o (dO V^T)/(1-p);  D_i = dO_i . O_i;
+ *   dS = P o (dP - D);  dQ = tau dS K;  dK = tau dS^T Q.
+ *   q,k,v,o,dout : device [B,H,N,d] inputs;  lse: device float32 [B,H,N]
+ *                  from fa_fwd with the same p
+ *   dq,dk,dv     : device [B,H,N,d] outputs (same dtype and strides)
+ *   ws           : device workspace, ws_bytes >= fa_bwd_workspace_size(p)
+ * ------------------------------------------------------------------------- */
+fa_status fa_bwd(const fa_params *p, const void *q, const void *k, const void *v,
+                 const void *o, const void *dout, const float *lse,
+                 void *dq, void *dk, void *dv, void *ws, size_t ws_bytes,
+                 void *stream);
+
+/* ---------------------------------------------------------------------------
+ * fa_check_status -- synchronises `stream`, then reads the status word the
+ * last fa_fwd/fa_bwd on `ws` left: FA_OK, or FA_ERR_TIMEOUT if a bounded
+ * device wait ran out (outputs are then undefined).  FA_ERR_CUDA if the
+ * stream reported an error.
+ * ------------------------------------------------------------------------- */
+fa_status fa_check_status(const void *ws, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * fa_dropout_mask -- writes the dropout keep-mask fa_fwd/fa_bwd use for rows
+ * row0 .. row0+nrows-1 of head (b, h): out[r][j] = 1 if kept, else 0, for
+ * j in [0, N).  out: device uint8 [nrows][N].  Same mapping as fa_fwd.
+ * For testing the mapping bit for bit; the attention kernels never store Z.
+ * ------------------------------------------------------------------------- */
+fa_status fa_dropout_mask(const fa_params *p, int32_t b, int32_t h, int32_t row0,
+                          int32_t nrows, uint8_t *out, void *stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *fa_status_string(fa_status s);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_GB300_FA_H */

@@ -143,8 +143,8 @@ def head_backward(spec: Spec, b, h, q, k, v, do, rows=None, cols=None):
     """Gradients of one head.
 
     Returns a dict with ``dq`` for query ``rows`` (default all), ``dk``/``dv``
-    for key ``cols`` (default all), and ``D`` for every row (D_i = sum_j
-    P_ij dP_ij, needed by any key column).
+    for key ``cols`` (default all), and ``D`` / ``lse`` (D_i = sum_j P_ij
+    dP_ij) for every row that the requested outputs depend on (NaN elsewhere).
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     N, d = q.shape
@@ -152,11 +152,19 @@ def head_backward(spec: Spec, b, h, q, k, v, do, rows=None, cols=None):
     allc = np.arange(N)
     rows = allc if rows is None else np.asarray(rows, dtype=np.int64)
     cols = allc if cols is None else np.asarray(cols, dtype=np.int64)
-    # D_i and LSE_i for every row (a key column sees every row).
-    D = np.zeros(N)
-    lse = np.zeros(N)
+    # D_i and LSE_i for every row that sees one of ``cols`` or is in ``rows``
+    # (any other row has P = 0 against the selected columns and contributes
+    # nothing to them); NaN marks rows that were not needed.
+    need = np.zeros(N, dtype=bool)
+    need[rows] = True
     for s in range(0, N, ROW_CHUNK):
         r = allc[s:s + ROW_CHUNK]
+        need[r] |= visible(spec, b, r, cols).any(axis=1)
+    D = np.full(N, np.nan)
+    lse = np.full(N, np.nan)
+    nr = allc[need]
+    for s in range(0, nr.size, ROW_CHUNK):
+        r = nr[s:s + ROW_CHUNK]
         _, _, _, D[r], lse[r] = _row_stats(spec, b, h, q, k, v, do, r, allc)
     # dQ rows: dQ_i = tau sum_j dS_ij K_j with dS = P o (dP - D).
     dq = np.zeros((rows.size, d))
@@ -168,8 +176,8 @@ def head_backward(spec: Spec, b, h, q, k, v, do, rows=None, cols=None):
     # dK, dV columns: sums over every row i.
     dk = np.zeros((cols.size, d))
     dv = np.zeros((cols.size, d))
-    for s in range(0, N, ROW_CHUNK):
-        r = allc[s:s + ROW_CHUNK]
+    for s in range(0, nr.size, ROW_CHUNK):
+        r = nr[s:s + ROW_CHUNK]
         vis = visible(spec, b, r, cols)
         S = tau * (q[r] @ k[cols].T)
         lr = lse[r][:, None]

@@ -1,0 +1,125 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path, run the oracle, compare.
+
+Tolerances (written here once, used by every parity test):
+  float32 inputs: max|dO| <= 1e-5 on O, |dLSE| <= 1e-5, relative Frobenius
+                  error <= 1e-5 for dQ, dK, dV.
+  16-bit inputs:  max|dO| <= 4e-3 on the kernel's float32 O (exported before
+                  the final rounding); the stored 16-bit O within 4e-3 plus
+                  half an ulp of the storage dtype at |O_ref|; |dLSE| <= 1e-3;
+                  relative Frobenius error <= 1e-2 for dQ, dK, dV.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from exact_io_aware_tiled_gb300 import workloads as W
+import exact_io_aware_tiled_gb300 as fa
+from oracle import attention as A
+
+TOL = {
+    "f32": dict(o=1e-5, lse=1e-5, grad=1e-5),
+    "f16": dict(o=4e-3, lse=1e-3, grad=1e-2),
+    "bf16": dict(o=4e-3, lse=1e-3, grad=1e-2),
+}
+MANT_BITS = {"f16": 10, "bf16": 7, "f32": 23}
+
+
+def half_ulp(x, dtype):
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(x, 1e-30)))
+    if dtype == "f16":
+        e = np.maximum(e, -14)
+    return 0.5 * np.exp2(e - MANT_BITS[dtype])
+
+
+def spec_of(wl: W.Workload) -> A.Spec:
+    return A.Spec(B=wl.B, H=wl.H, N=wl.N, d=wl.d, causal=wl.causal,
+                  seqlens_k=None if wl.seqlens is None else np.asarray(wl.seqlens),
+                  block_mask=None if wl.block_mask is None else wl.block_mask.astype(bool),
+                  block_size=wl.block_size, dropout_p=wl.dropout_p, seed=wl.dropout_seed,
+                  offset=wl.dropout_offset)
+
+
+def kwargs_of(wl: W.Workload):
+    return dict(causal=wl.causal,
+                seqlens_k=None if wl.seqlens is None else torch.from_numpy(np.asarray(wl.seqlens, dtype=np.int32)),
+                dropout_p=wl.dropout_p, seed=wl.dropout_seed, offset=wl.dropout_offset,
+                block_mask=None if wl.block_mask is None else torch.from_numpy(wl.block_mask.astype(np.uint8)))
+
+
+def run_gpu(wl: W.Workload, inputs, layout="bhnd", want_o32=True):
+    """fwd + bwd through the C ABI; returns numpy float64 copies of everything."""
+    dev = torch.device("cuda:0")
+    t = {k: v.to(dev) for k, v in inputs.items()}
+    if layout == "bnhd":   # non-contiguous strides: [B, N, H, d] memory viewed as [B, H, N, d]
+        t = {k: v.transpose(1, 2).contiguous().transpose(1, 2) for k, v in t.items()}
+    kw = kwargs_of(wl)
+    want_o32 = want_o32 and wl.dtype != "f32"
+    out = fa.fwd(t["q"], t["k"], t["v"], return_o_f32=want_o32, **kw)
+    o, lse = out[0], out[1]
+    st = fa.check_status(fa.fwd.last_workspace)
+    assert st == 0, "fa_fwd device status %d" % st
+    res = dict(o=o, lse=lse, o32=out[2] if want_o32 else None)
+    if "do" in t:
+        dq, dk, dv = fa.bwd(t["q"], t["k"], t["v"], o, t["do"], lse, **kw)
+        st = fa.check_status(fa.bwd.last_workspace)
+        assert st == 0, "fa_bwd device status %d" % st
+        res.update(dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    return {k: (None if v is None else v.float().cpu().numpy().astype(np.float64)) for k, v in res.items()}
+
+
+def np64(t):
+    return t.float().numpy().astype(np.float64)
+
+
+def rel_frob(a, b):
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
+
+
+def check_head(wl, inputs, got, b, h, rows=None, cols=None, do_grads=True):
+    """Compare one head (optionally sampled rows / cols) with the oracle."""
+    spec = spec_of(wl)
+    tol = TOL[wl.dtype]
+    q, k, v = (np64(inputs[n][b, h]) for n in ("q", "k", "v"))
+    rr = np.arange(wl.N) if rows is None else np.asarray(rows)
+    cc = np.arange(wl.N) if cols is None else np.asarray(cols)
+    O, L = A.head_forward(spec, b, h, q, k, v, rows=rr)
+    report = {}
+    lse_g = got["lse"][b, h][rr]
+    fin = np.isfinite(L)
+    assert np.array_equal(np.isfinite(lse_g), fin), "LSE finiteness differs"
+    report["lse"] = float(np.max(np.abs(lse_g[fin] - L[fin]), initial=0.0))
+    assert report["lse"] <= tol["lse"], report
+    o_g = got["o"][b, h][rr]
+    if wl.dtype == "f32":
+        report["o"] = float(np.max(np.abs(o_g - O), initial=0.0))
+        assert report["o"] <= tol["o"], report
+    else:
+        o32 = got["o32"][b, h][rr]
+        report["o32"] = float(np.max(np.abs(o32 - O), initial=0.0))
+        assert report["o32"] <= tol["o"], report
+        excess = np.abs(o_g - O) - (tol["o"] + half_ulp(O, wl.dtype))
+        report["o_stored_excess"] = float(np.max(excess, initial=-1.0))
+        assert report["o_stored_excess"] <= 0.0, report
+    if do_grads and "dq" in got:
+        do = np64(inputs["do"][b, h])
+        g = A.head_backward(spec, b, h, q, k, v, do, rows=rr, cols=cc)
+        for name, ref, gg in (("dq", g["dq"], got["dq"][b, h][rr]), ("dk", g["dk"], got["dk"][b, h][cc]),
+                              ("dv", g["dv"], got["dv"][b, h][cc])):
+            report[name] = rel_frob(gg, ref)
+            assert report[name] <= tol["grad"], (name, report)
+    return report
+
+
+def sample_rows(N, seed, extra=256):
+    rng = np.random.default_rng(seed)
+    s = set(range(min(128, N))) | set(range(max(0, N - 128), N))
+    for t in range(128, N, 128):
+        s |= {t - 1, t}
+        if t + 1 < N:
+            s.add(t + 1)
+    s |= set(rng.integers(0, N, size=min(extra, N)).tolist())
+    return np.array(sorted(s))

@@ -1,0 +1,146 @@
+"""C-ABI checks that need no GPU: exports, struct layout, host-side validation."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import exact_io_aware_tiled_gb300 as fa
+    fa.build()
+    return fa.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["fa_fwd", "fa_bwd", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_check_status",
+              "fa_dropout_mask", "fa_status_string", "fa_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    nm = shutil.which("nm")
+    from exact_io_aware_tiled_gb300 import LIB
+    if nm:
+        out = subprocess.run([nm, "-D", "--defined-only", str(LIB)], capture_output=True, text=True).stdout
+        exported = set(re.findall(r"\bT (fa_[a-z0-9_]+)\b", out))
+    else:  # pragma: no cover
+        exported = {n for n in declared_functions() if hasattr(lib, n)}
+    for n in declared_functions():
+        assert n in exported, n
+        assert getattr(lib, n) is not None
+
+
+def test_params_struct_layout_matches_c(tmp_path):
+    from exact_io_aware_tiled_gb300._lib import fa_params
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    fields = [f for f, _ in fa_params._fields_]
+    prog = ['#include <stdio.h>', '#include <stddef.h>', '#include "fa.h"', 'int main(void){',
+            'printf("%zu\\n", sizeof(fa_params));']
+    prog += ['printf("%%zu\\n", offsetof(fa_params, %s));' % f for f in fields]
+    prog += ['return 0;}']
+    c = tmp_path / "layout.c"
+    c.write_text("\n".join(prog))
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), str(c), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(fa_params)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(fa_params, f).offset == off, f
+
+
+def _params(**kw):
+    from exact_io_aware_tiled_gb300._lib import fa_params
+    p = fa_params()
+    p.B, p.H, p.N, p.d, p.dtype = 2, 3, 200, 64, 2
+    p.stride_n, p.stride_h, p.stride_b = 64, 200 * 64, 3 * 200 * 64
+    p.block_size = 128
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_status_strings(lib):
+    assert lib.fa_status_string(0) == b"FA_OK"
+    assert lib.fa_status_string(6) == b"FA_ERR_TIMEOUT"
+    assert lib.fa_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    p = _params()
+    f = lib.fa_fwd_workspace_size(ctypes.byref(p))
+    b = lib.fa_bwd_workspace_size(ctypes.byref(p))
+    assert f >= 4
+    # bwd holds the float32 dQ accumulator and the padded LSE / D rows
+    assert b >= 2 * 3 * 200 * 64 * 4 + 2 * 2 * 3 * 256 * 4
+    p32 = _params(dtype=0)
+    assert lib.fa_bwd_workspace_size(ctypes.byref(p32)) < b
+
+
+FAKE = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("mut,code", [
+    (dict(d=128), 2),                 # head dim 128 not built yet -> UNSUPPORTED
+    (dict(d=0), 1),
+    (dict(N=0), 1),
+    (dict(dtype=7), 1),
+    (dict(stride_n=68), 3),           # 68 * 2 bytes is not a multiple of 16
+    (dict(dropout_p=1.0), 1),
+    (dict(dropout_p=-0.1), 1),
+    (dict(block_mask=1 << 20, block_size=64), 2),
+])
+def test_host_validation_rejects_before_launch(lib, mut, code):
+    p = _params(**mut)
+    ws = ctypes.c_void_p(1 << 21)
+    st = lib.fa_fwd(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, ws, 1 << 30, None)
+    assert st == code
+
+
+def test_null_and_misaligned_pointers_and_small_workspace(lib):
+    p = _params()
+    ws = ctypes.c_void_p(1 << 21)
+    assert lib.fa_fwd(None, FAKE, FAKE, FAKE, FAKE, FAKE, ws, 1 << 30, None) == 1
+    assert lib.fa_fwd(ctypes.byref(p), None, FAKE, FAKE, FAKE, FAKE, ws, 1 << 30, None) == 1
+    assert lib.fa_fwd(ctypes.byref(p), ctypes.c_void_p((1 << 20) + 8), FAKE, FAKE, FAKE, FAKE, ws, 1 << 30,
+                      None) == 3
+    assert lib.fa_fwd(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, ws, 16, None) == 4
+    assert lib.fa_fwd(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, None, 1 << 30, None) == 4
+    assert lib.fa_bwd(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, ws, 1 << 30,
+                      None) == 1
+    assert lib.fa_bwd(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, 16, None) == 4
+    assert lib.fa_dropout_mask(ctypes.byref(p), 2, 0, 0, 1, FAKE, None) == 1      # b out of range
+    assert lib.fa_dropout_mask(ctypes.byref(p), 0, 0, 190, 20, FAKE, None) == 1   # rows past N
+
+
+def test_product_path_refuses_to_run_without_library(tmp_path, monkeypatch):
+    import exact_io_aware_tiled_gb300._lib as L
+    monkeypatch.setattr(L, "_lib", None)
+    monkeypatch.setattr(L, "_LIB_PATH", tmp_path / "missing.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        L.load()
+
+
+def test_binding_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "exact_io_aware_tiled_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), f
+                assert "oracle." not in src or f.endswith((".cu", ".cuh", ".h")), f

@@ -1,0 +1,118 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Small cases are compared element by element on whole heads; they span
+several tiles, ragged tails and every mask.  See tests/parity.py for the
+tolerances.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from exact_io_aware_tiled_gb300 import workloads as W
+import exact_io_aware_tiled_gb300 as fa
+from oracle import philox
+from tests.parity import check_head, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    fa.build()
+    fa.load()
+
+
+def _wl(N, dtype="bf16", B=2, H=3, seed=7, **kw):
+    return W.Workload("case", B=B, H=H, N=N, dtype=dtype, seed=seed, **kw)
+
+
+def _check_all_heads(wl, layout="bhnd"):
+    inp = W.make_inputs(wl)
+    got = run_gpu(wl, inp, layout=layout)
+    worst = {}
+    for b in range(wl.B):
+        for h in range(wl.H):
+            r = check_head(wl, inp, got, b, h)
+            for k, v in r.items():
+                worst[k] = max(worst.get(k, -1e9), v)
+    return worst
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("N", [1, 127, 128, 129, 255, 256, 300])
+def test_dense(dtype, N):
+    _check_all_heads(_wl(N, dtype))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("N", [1, 128, 129, 300, 513])
+def test_causal(dtype, N):
+    _check_all_heads(_wl(N, dtype, causal=True))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_key_padding_including_empty_and_single_key(dtype):
+    wl = _wl(300, dtype, B=4, H=2, seqlens=np.array([0, 1, 300, 157], dtype=np.int32))
+    _check_all_heads(wl)
+    _check_all_heads(wl.with_(causal=True))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("p", [0.1, 0.5])
+def test_dropout(dtype, p):
+    _check_all_heads(_wl(257, dtype, dropout_p=p, dropout_seed=0xDEADBEEF12345, dropout_offset=3))
+
+
+def test_dropout_with_padding_and_causal():
+    wl = _wl(384, "bf16", B=2, H=2, causal=True, dropout_p=0.2, seqlens=np.array([200, 384], dtype=np.int32))
+    _check_all_heads(wl)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_block_sparse_butterfly(dtype):
+    _check_all_heads(_wl(1024, dtype, B=1, H=2, sparse_butterfly=True))
+
+
+def test_block_sparse_random_mask_with_empty_rows_and_causal():
+    rng = np.random.default_rng(3)
+    bm = (rng.random((5, 5)) < 0.4).astype(np.uint8)
+    bm[2, :] = 0                      # a query block with no visible key at all
+    for causal in (False, True):
+        _check_all_heads(_wl(600, "bf16", B=1, H=2, block_mask=bm, causal=causal))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_non_contiguous_layout(dtype):
+    _check_all_heads(_wl(200, dtype, causal=True), layout="bnhd")
+
+
+def test_forward_p_through_shared_memory_variant(monkeypatch):
+    # the alternative build of the forward kernel that stages P in shared memory
+    monkeypatch.setenv("FA_FWD_P_SMEM", "1")
+    _check_all_heads(_wl(300, "bf16", causal=True))
+    _check_all_heads(_wl(257, "f16", dropout_p=0.3))
+
+
+def test_dropout_mask_bit_exact():
+    B, H, N = 3, 5, 1000
+    for (b, h, row0, nrows, p, seed, off) in [(0, 0, 0, 64, 0.1, 0x5EED, 0), (2, 4, 900, 100, 0.5, 2**63 + 5, 2**40),
+                                              (1, 3, 17, 33, 0.9, 12345, 7)]:
+        got = fa.dropout_mask(B, H, N, b, h, row0, nrows, dropout_p=p, seed=seed, offset=off).cpu().numpy()
+        ref = philox.keep_mask(B, H, N, b, h, np.arange(row0, row0 + nrows), p, seed, off)
+        assert np.array_equal(got.astype(bool), ref)
+
+
+def test_repeated_calls_are_deterministic_in_forward():
+    wl = _wl(300, "bf16", causal=True)
+    inp = W.make_inputs(wl, grads=False)
+    a = run_gpu(wl, inp)
+    b = run_gpu(wl, inp)
+    assert np.array_equal(a["o"], b["o"]) and np.array_equal(a["lse"], b["lse"])
+
+
+def test_host_errors_are_raised_not_hidden():
+    q = torch.zeros((1, 1, 64, 128), device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(fa.FAError):
+        fa.fwd(q, q, q)
