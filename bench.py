@@ -1,0 +1,376 @@
+"""Benchmark: one step = forward + backward attention over one batch.
+
+Default workload: the GPT-2-medium-shaped causal attention (B=64, H=16,
+N=1024, d=64, bf16).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+FLOP convention (FlashAttention pages; exact count of unmasked (i, j) pairs):
+  forward = 4 d per visible pair (Q K^T and P V);
+  "fwd+bwd" headline = 2.5 x forward (the literal reading of the metric);
+  executed fwd+bwd = forward + backward (10 d per pair: S recompute, dP, dV,
+  dK, dQ) = 3.5 x forward, reported beside it.
+Multi-GPU: every rank runs its own full copy of the workload (independent
+heads, no collective on the data path); value = all ranks' FLOPs / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd attention TFLOP/s & % of BF16 tensor peak, GPT-2-medium shape"
+
+
+def visible_pairs(wl) -> int:
+    """Exact number of visible (query, key) pairs summed over all heads."""
+    N, T = wl.N, 128
+    nb = -(-N // T)
+    if wl.block_mask is not None:
+        blocks = np.argwhere(wl.block_mask != 0)
+    else:
+        blocks = np.array([(I, J) for I in range(nb) for J in range(nb)])
+    Ls = [N] * wl.B if wl.seqlens is None else [int(min(max(x, 0), N)) for x in wl.seqlens]
+    total = 0
+    for L in Ls:
+        cnt = 0
+        for I, J in blocks:
+            i = np.arange(I * T, min(N, I * T + T))
+            jlo, jhi = J * T, min(N, L, J * T + T)          # keys [jlo, jhi)
+            if jhi <= jlo:
+                continue
+            if wl.causal:
+                cnt += int(np.clip(np.minimum(i + 1, jhi) - jlo, 0, None).sum())
+            else:
+                cnt += i.size * (jhi - jlo)
+        total += cnt * wl.H
+    return total
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.proc = None
+        self.lines = []
+        self.idx = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        time.sleep(0.1)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [x for x in sm if smax is None or x > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(wl, budget_s, inputs=None):
+    """Time the float64 oracle (as it stands) on whole heads of `wl` for ~budget_s."""
+    from oracle import attention as A
+    from exact_io_aware_tiled_gb300 import workloads as W
+    spec = A.Spec(B=wl.B, H=wl.H, N=wl.N, d=wl.d, causal=wl.causal,
+                  seqlens_k=None if wl.seqlens is None else np.asarray(wl.seqlens),
+                  block_mask=None if wl.block_mask is None else wl.block_mask.astype(bool),
+                  dropout_p=wl.dropout_p, seed=wl.dropout_seed, offset=wl.dropout_offset)
+    one = wl.with_(B=1, H=1, seqlens=None if wl.seqlens is None else wl.seqlens[:1])
+    inp = W.make_inputs(one) if inputs is None else inputs
+    q, k, v, do = (inp[n][0, 0].float().numpy().astype(np.float64) for n in ("q", "k", "v", "do"))
+    head_flops = 2.5 * 4 * wl.d * visible_pairs(one)
+    t0 = time.perf_counter()
+    heads = 0
+    while True:
+        A.head_forward(spec, 0, 0, q, k, v)
+        A.head_backward(spec, 0, 0, q, k, v, do)
+        heads += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return heads * head_flops / dt / 1e12, heads, dt
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, wl):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(wl, 0.0)
+    vals = []
+    t0 = time.perf_counter()
+    heads_total = 0
+    for _ in range(args.steps):
+        v, heads, _ = oracle_sample(wl, 0.0)
+        vals.append(v)
+        heads_total += heads
+    dt = time.perf_counter() - t0
+    value = float(np.mean(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "causal": wl.causal,
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": "one (b=0,h=0) head fwd+bwd per step, float64 numpy, %d heads total" % heads_total},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gpt2_medium_causal")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--batch", type=int, default=0, help="override B (small profiling cases)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from exact_io_aware_tiled_gb300 import workloads as W
+    wl = W.CONFIGS[args.workload]
+    if args.batch > 0:
+        wl = wl.with_(B=args.batch, name=wl.name + "_B%d" % args.batch,
+                      seqlens=None if wl.seqlens is None else wl.seqlens[:args.batch])
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    import exact_io_aware_tiled_gb300 as fa
+    fa.load()
+
+    host = W.make_inputs(wl)
+    t = {k: v.to(dev) for k, v in host.items()}
+    kw = dict(causal=wl.causal, dropout_p=wl.dropout_p, seed=wl.dropout_seed, offset=wl.dropout_offset,
+              seqlens_k=None if wl.seqlens is None else torch.from_numpy(np.asarray(wl.seqlens, np.int32)).to(dev),
+              block_mask=None if wl.block_mask is None else torch.from_numpy(wl.block_mask.astype(np.uint8)).to(dev))
+    pairs = visible_pairs(wl)
+    fwd_flops = 4.0 * wl.d * pairs
+    bwd_flops = 10.0 * wl.d * pairs
+    step_flops_headline = 2.5 * fwd_flops
+    step_flops_exec = fwd_flops + bwd_flops
+    stream = torch.cuda.current_stream(dev)
+
+    def step(prof_f=None, prof_b=None):
+        o, lse = fa.fwd(t["q"], t["k"], t["v"], prof=prof_f, **kw)
+        dq, dk, dv = fa.bwd(t["q"], t["k"], t["v"], o, t["do"], lse, prof=prof_b, **kw)
+        return o, lse, dq
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st_f = fa.check_status(fa.fwd.last_workspace)
+    st_b = fa.check_status(fa.bwd.last_workspace)
+    if st_f or st_b:
+        raise SystemExit("device status after warm-up: fwd %d bwd %d" % (st_f, st_b))
+
+    K = args.steps
+    evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in evf + evb:      # materialise the events so their handles can be passed down
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(dev.index)
+    clk.start()
+    time.sleep(0.3)
+    _barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for s in range(K):
+        step((evf[s][0].cuda_event, evf[s][1].cuda_event), (evb[s][0].cuda_event, evb[s][1].cuda_event))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    clocks = clk.stop()
+    ms = e0.elapsed_time(e1) / K
+    fwd_ms = sum(a.elapsed_time(b) for a, b in evf) / K
+    bwd_ms = sum(a.elapsed_time(b) for a, b in evb) / K
+    ms_max = _max_over_ranks(ms, ws, dev)
+
+    # end to end: pinned host inputs -> device, fwd + bwd, gradients and O back to pinned host
+    e2e = None
+    if not args.no_e2e:
+        hp = {k: v.pin_memory() for k, v in host.items()}
+        outs = {n: torch.empty_like(hp["q"]).pin_memory() for n in ("o", "dq", "dk", "dv")}
+        lse_h = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in hp.values())
+        d2h = sum(v.numel() * v.element_size() for v in outs.values()) + lse_h.numel() * 4
+
+        def e2e_step():
+            d = {k: v.to(dev, non_blocking=True) for k, v in hp.items()}
+            o, lse = fa.fwd(d["q"], d["k"], d["v"], **kw)
+            dq, dk, dv = fa.bwd(d["q"], d["k"], d["v"], o, d["do"], lse, **kw)
+            for n, x in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+                outs[n].copy_(x, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        _barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        KE = max(3, K // 2)
+        a.record(stream)
+        for _ in range(KE):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = _max_over_ranks(a.elapsed_time(b) / KE, ws, dev)
+        e2e = {"value": ws * step_flops_headline / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    peaks, peak_kind = _peaks()
+    dominant = "bwd" if bwd_ms >= fwd_ms else "fwd"
+    kern_ms = bwd_ms if dominant == "bwd" else fwd_ms
+    kern_flops = bwd_flops if dominant == "bwd" else fwd_flops
+    achieved = kern_flops / (kern_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops_sustained"])
+    traffic = _recorded_traffic(wl.name, dominant)
+
+    if rank != 0:
+        return
+    cpu = None
+    if ws == 1 and args.cpu_budget > 0:
+        v, heads, dt = oracle_sample(wl, args.cpu_budget)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+               "sample": "%d whole (b=0,h=0) heads fwd+bwd in %.1f s, float64 numpy" % (heads, dt)}
+    value = ws * step_flops_headline / (ms_max * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "causal": wl.causal,
+                   "dropout_p": wl.dropout_p, "parallelism": "replicas" if ws > 1 else "single",
+                   "l2": "inputs exceed L2 (%.0f MB per step)" % (sum(v.numel() * v.element_size()
+                                                                      for v in host.values()) / 1e6)},
+        "pct_of_bf16_peak": 100.0 * value / float(peaks["bf16_tflops_sustained"]) / ws,
+        "value_executed_flops": ws * step_flops_exec / (ms_max * 1e-3) / 1e12,
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "roofline": {"kernel": "attn_%s_tc" % dominant, "bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": "%s bf16_tflops_sustained" % peak_kind},
+        "roofline_fwd": {"achieved": fwd_flops / (fwd_ms * 1e-3) / 1e12, "peak": peak,
+                         "frac": fwd_flops / (fwd_ms * 1e-3) / 1e12 / peak},
+        "clocks": clocks,
+        "gpu_launches": _launches_per_step(wl) * K,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _launches_per_step(wl):
+    # fwd: [block lists] + attention; bwd: [block lists] + prep + attention + dq convert (16-bit)
+    sparse = 1 if wl.block_mask is not None else 0
+    fwd = sparse + 1
+    bwd = sparse + 2 + (0 if wl.dtype == "f32" else 1)
+    return fwd + bwd
+
+
+def _recorded_traffic(workload, which):
+    """DRAM bytes per launch recorded from an ncu capture of the current kernel (profiles/traffic.json)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    return d.get(workload, {}).get(which)
+
+
+if __name__ == "__main__":
+    main()

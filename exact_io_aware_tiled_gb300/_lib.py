@@ -37,6 +37,7 @@ class fa_params(ctypes.Structure):
         ("block_mask", ctypes.c_void_p),
         ("block_size", ctypes.c_int32),
         ("o_f32", ctypes.c_void_p),
+        ("prof_start", ctypes.c_void_p), ("prof_stop", ctypes.c_void_p),
     ]
 
 
@@ -95,7 +96,7 @@ def _stream(stream):
 
 
 def make_params(q: torch.Tensor, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0,
-                block_mask=None, scale=None, o_f32=None) -> fa_params:
+                block_mask=None, scale=None, o_f32=None, prof=None) -> fa_params:
     B, H, N, d = q.shape
     p = fa_params()
     p.B, p.H, p.N, p.d = B, H, N, d
@@ -110,6 +111,8 @@ def make_params(q: torch.Tensor, *, causal=False, seqlens_k=None, dropout_p=0.0,
     p.block_mask = None if block_mask is None else block_mask.data_ptr()
     p.block_size = 128
     p.o_f32 = None if o_f32 is None else o_f32.data_ptr()
+    if prof is not None:
+        p.prof_start, p.prof_stop = prof
     return p
 
 
@@ -147,7 +150,7 @@ def _aux(seqlens_k, block_mask, q):
 
 
 def fwd(q, k, v, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0, block_mask=None,
-        scale=None, return_o_f32=False, stream=None):
+        scale=None, return_o_f32=False, stream=None, prof=None):
     """O, LSE (and optionally the float32 O before rounding) via fa_fwd."""
     _check(q)
     q, k, v = _same_layout([q, k, v])
@@ -158,7 +161,7 @@ def fwd(q, k, v, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
     o32 = torch.empty((B, H, N, d), device=q.device, dtype=torch.float32) if return_o_f32 else None
     p = make_params(q, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
-                    block_mask=block_mask, scale=scale, o_f32=o32)
+                    block_mask=block_mask, scale=scale, o_f32=o32, prof=prof)
     wsz = lib.fa_fwd_workspace_size(ctypes.byref(p))
     ws = torch.empty(wsz, device=q.device, dtype=torch.uint8)
     st = lib.fa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), wsz, _stream(stream))
@@ -169,7 +172,7 @@ def fwd(q, k, v, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=
 
 
 def bwd(q, k, v, o, do, lse, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0, block_mask=None,
-        scale=None, stream=None):
+        scale=None, stream=None, prof=None):
     """dQ, dK, dV via fa_bwd."""
     _check(q)
     q, k, v, o, do = _same_layout([q, k, v, o, do])
@@ -178,7 +181,7 @@ def bwd(q, k, v, o, do, lse, *, causal=False, seqlens_k=None, dropout_p=0.0, see
     lse = lse.contiguous()
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     p = make_params(q, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
-                    block_mask=block_mask, scale=scale)
+                    block_mask=block_mask, scale=scale, prof=prof)
     wsz = lib.fa_bwd_workspace_size(ctypes.byref(p))
     ws = torch.empty(wsz, device=q.device, dtype=torch.uint8)
     st = lib.fa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),

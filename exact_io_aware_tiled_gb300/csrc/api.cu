@@ -161,6 +161,19 @@ fa_status prepare_common(const fa_params* p, const Layout& L, uint8_t* ws, cudaS
   return cuda_status(e);
 }
 
+// Records the caller's optional profiling events around the main kernel.
+struct ProfScope {
+  cudaEvent_t a, b;
+  cudaStream_t s;
+  ProfScope(const fa_params* p, cudaStream_t st)
+      : a((cudaEvent_t)p->prof_start), b((cudaEvent_t)p->prof_stop), s(st) {
+    if (a && b) cudaEventRecord(a, s);
+  }
+  ~ProfScope() {
+    if (a && b) cudaEventRecord(b, s);
+  }
+};
+
 bool fwd_p_in_tmem() {
   const char* v = std::getenv("FA_FWD_P_SMEM");
   return !(v != nullptr && v[0] == '1');
@@ -209,12 +222,14 @@ fa_status fa_fwd(const fa_params* p, const void* q, const void* k, const void* v
   if ((s = prepare_common(p, L, w, st)) != FA_OK) return s;
   if (p->dtype == FA_DT_F32) {
     if (p->o_f32 != nullptr) return FA_ERR_UNSUPPORTED;   // O is already float32
+    ProfScope prof(p, st);
     return cuda_status(launch_fwd_simt((const float*)q, (const float*)k, (const float*)v, (float*)o, sd, a, st));
   }
   CUtensorMap mq, mk, mv, mo;
   if ((s = map16(&mq, q, p, sd)) != FA_OK || (s = map16(&mk, k, p, sd)) != FA_OK ||
       (s = map16(&mv, v, p, sd)) != FA_OK || (s = map16(&mo, o, p, sd)) != FA_OK)
     return s;
+  ProfScope prof(p, st);
   return cuda_status(launch_fwd_tc(p->dtype, fwd_p_in_tmem(), mq, mk, mv, mo, a, st));
 }
 
@@ -250,9 +265,11 @@ fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v
                                   reinterpret_cast<float*>(w + L.lse2), reinterpret_cast<float*>(w + L.dvec), dqacc,
                                   st);
   if (e != cudaSuccess) return FA_ERR_CUDA;
-  if (p->dtype == FA_DT_F32)
+  if (p->dtype == FA_DT_F32) {
+    ProfScope prof(p, st);
     return cuda_status(launch_bwd_simt((const float*)q, (const float*)k, (const float*)v, (const float*)dout,
                                        (float*)dq, (float*)dk, (float*)dv, sd, a, st));
+  }
   CUtensorMap mq, mk, mv, mdo, mdk, mdv, macc;
   Strides acc_st{(int64_t)p->H * p->N * kHeadDim, (int64_t)p->N * kHeadDim, kHeadDim};
   if ((s = map16(&mq, q, p, sd)) != FA_OK || (s = map16(&mk, k, p, sd)) != FA_OK ||
@@ -260,7 +277,10 @@ fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v
       (s = map16(&mdk, dk, p, sd)) != FA_OK || (s = map16(&mdv, dv, p, sd)) != FA_OK ||
       (s = make_map(&macc, dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kHeadDim, 32, p, acc_st)) != FA_OK)
     return s;
-  if ((e = launch_bwd_tc(p->dtype, mq, mk, mv, mdo, mdk, mdv, macc, a, st)) != cudaSuccess) return FA_ERR_CUDA;
+  {
+    ProfScope prof(p, st);
+    if ((e = launch_bwd_tc(p->dtype, mq, mk, mv, mdo, mdk, mdv, macc, a, st)) != cudaSuccess) return FA_ERR_CUDA;
+  }
   return cuda_status(launch_dq_convert(p->dtype, dqacc, dq, sd, p->B, p->H, p->N, st));
 }
 

@@ -79,6 +79,10 @@ typedef struct {
   float *o_f32;              /* optional device [B,H,N,d] contiguous float32:
                                 fa_fwd also writes O before its final rounding
                                 to the storage dtype (parity diagnostics)       */
+  void *prof_start;          /* optional cudaEvent_t pair: when both are set,   */
+  void *prof_stop;           /* they are recorded on `stream` right before and
+                                right after the main attention kernel of the
+                                call (profiling; not owned by the library)      */
 } fa_params;
 
 /* ---------------------------------------------------------------------------
