@@ -276,17 +276,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
       // mask (only boundary tiles) and row max of the raw scores
       const int jl = jmax - kv * kTile;
-      float mx = -INFINITY;
-      if (jl >= kTile - 1) {
+      if (jl < kTile - 1) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
+        for (int c = 0; c < 128; ++c)
           if (c > jl) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-          mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
-        }
       }
+      // row max as 8 independent chains (latency), then a short tree
+      float m8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) m8[t] = __uint_as_float(sr[0][t]);
+#pragma unroll
+      for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       mx *= sl2;
       // running reference max: moved only when the tile max exceeds it by 2^8
       float m_new = m_run;
@@ -306,8 +307,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           keep[g >> 2] = (g & 3) == 0 ? bits : (keep[g >> 2] | (bits << ((g & 3) * 8)));
         }
       }
-      // P = exp2(S * tau*log2e - m) in two halves of 64 keys (32 packed words)
-      float lt0 = 0.f, lt1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+      // P = exp2(S * tau*log2e - m) in two halves of 64 keys (32 packed words).
+      // l_true sums the unrounded P (for the logsumexp); l_rnd sums exactly the
+      // 16-bit values the PV MMA consumes before dropout zeroes some of them
+      // (P, or P/(1-p) with dropout), so O / l_rnd is a consistently rounded
+      // convex combination of V rows.
+      const float pscale = a.drop.enabled ? a.drop.rp : 1.f;
+      float lt[4] = {0.f, 0.f, 0.f, 0.f}, lr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t pk[32];
@@ -316,15 +322,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           const int c = hf * 64 + c2;
           const float p0 = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -mref));
           const float p1 = ex2(fmaf(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2, -mref));
-          lt0 += p0;
-          lt1 += p1;
-          uint32_t u = Cvt<T>::pack(p0, p1);
-          lr0 += Cvt<T>::lo(u);
-          lr1 += Cvt<T>::hi(u);
+          lt[(c >> 1) & 1] += p0;
+          lt[2 + ((c >> 1) & 1)] += p1;
+          uint32_t u = a.drop.enabled ? Cvt<T>::pack(p0 * pscale, p1 * pscale) : Cvt<T>::pack(p0, p1);
+          lr[(c >> 1) & 1] += Cvt<T>::lo(u);
+          lr[2 + ((c >> 1) & 1)] += Cvt<T>::hi(u);
           if (a.drop.enabled) {
-            const bool k0 = (keep[c >> 5] >> (c & 31)) & 1u;
-            const bool k1 = (keep[c >> 5] >> ((c + 1) & 31)) & 1u;
-            u = Cvt<T>::pack(k0 ? p0 * a.drop.rp : 0.f, k1 ? p1 * a.drop.rp : 0.f);
+            const uint32_t kb = keep[c >> 5] >> (c & 31);
+            u &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
           }
           pk[c2 >> 1] = u;
         }
@@ -341,6 +346,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           }
         }
       }
+      const float lt0 = lt[0] + lt[1], lt1 = lt[2] + lt[3];
+      const float lr0 = (lr[0] + lr[1]) / pscale, lr1 = (lr[2] + lr[3]) / pscale;
       l_true += lt0 + lt1;
       l_rnd += lr0 + lr1;
 

@@ -7,6 +7,12 @@ Tolerances (written here once, used by every parity test):
                   the final rounding); the stored 16-bit O within 4e-3 plus
                   half an ulp of the storage dtype at |O_ref|; |dLSE| <= 1e-3;
                   relative Frobenius error <= 1e-2 for dQ, dK, dV.
+With dropout the 16-bit O bound widens by the first-order effect of rounding
+the MMA input P~ = Z o P / (1 - p) to the storage dtype (unit roundoff u =
+2^-8 for bf16, 2^-11 for fp16): |dO_ic| <= 4e-3 + u * sum_j P~_ij |V_jc|.
+Without dropout the kernel normalises by the sum of the rounded P it fed to
+the MMA, the rounding errors cancel to first order and the plain 4e-3 holds;
+with dropout the dropped terms break that cancellation.
 Relative Frobenius error is ||G - G_ref|| / max(||G_ref||, floor).  The floor
 matters only where the exact gradient cancels to (nearly) zero -- e.g. a row
 with a single visible key has dS = P (dP - D) = 0 exactly, so dQ and dK vanish
@@ -31,6 +37,7 @@ TOL = {
     "bf16": dict(o=4e-3, lse=1e-3, grad=1e-2),
 }
 MANT_BITS = {"f16": 10, "bf16": 7, "f32": 23}
+UNIT_ROUNDOFF = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8, "f32": 2.0 ** -24}
 
 
 def half_ulp(x, dtype):
@@ -120,10 +127,15 @@ def check_head(wl, inputs, got, b, h, rows=None, cols=None, do_grads=True):
         report["o"] = float(np.max(np.abs(o_g - O), initial=0.0))
         assert report["o"] <= tol["o"], report
     else:
+        bound = np.full_like(O, tol["o"])
+        if wl.dropout_p > 0:
+            O_abs, _ = A.head_forward(spec, b, h, q, k, np.abs(v), rows=rr)   # sum_j P~_ij |V_jc|
+            bound = bound + UNIT_ROUNDOFF[wl.dtype] * O_abs
         o32 = sel("o32", rr_t)
         report["o32"] = float(np.max(np.abs(o32 - O), initial=0.0))
-        assert report["o32"] <= tol["o"], report
-        excess = np.abs(o_g - O) - (tol["o"] + half_ulp(O, wl.dtype))
+        report["o32_excess"] = float(np.max(np.abs(o32 - O) - bound, initial=-1.0))
+        assert report["o32_excess"] <= 0.0, report
+        excess = np.abs(o_g - O) - (bound + half_ulp(O, wl.dtype))
         report["o_stored_excess"] = float(np.max(excess, initial=-1.0))
         assert report["o_stored_excess"] <= 0.0, report
     if do_grads and "dq" in got:

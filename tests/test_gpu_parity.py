@@ -109,7 +109,7 @@ def test_repeated_calls_are_deterministic_in_forward():
     inp = W.make_inputs(wl, grads=False)
     a = run_gpu(wl, inp)
     b = run_gpu(wl, inp)
-    assert np.array_equal(a["o"], b["o"]) and np.array_equal(a["lse"], b["lse"])
+    assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
 
 
 def test_host_errors_are_raised_not_hidden():
