@@ -214,3 +214,27 @@ def dropout_mask(B, H, N, b, h, row0, nrows, *, dropout_p, seed=0, offset=0, dev
 
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
+
+
+def bwd_noalloc(q, k, v, o, do, lse, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0,
+                block_mask=None, scale=None, stream=None):
+    """dQ, dK, dV via fa_bwd_noalloc: the backward pass using the library's own
+    fixed device scratch array instead of a caller-allocated workspace (for
+    callers that cannot allocate device memory; problems needing more than
+    64 MiB of scratch are refused)."""
+    _check(q)
+    q, k, v, o, do = _same_layout([q, k, v, o, do])
+    lib = load()
+    fn = lib.fa_bwd_noalloc
+    fn.argtypes = [ctypes.POINTER(fa_params)] + [ctypes.c_void_p] * 10
+    fn.restype = ctypes.c_int
+    seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
+    lse = lse.contiguous()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    p = make_params(q, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
+                    block_mask=block_mask, scale=scale)
+    st = fn(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+            _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd_noalloc")
+    return dq, dk, dv

@@ -137,6 +137,32 @@ fa_status fa_bwd(const fa_params *p, const void *q, const void *k, const void *v
                  void *stream);
 
 /* ---------------------------------------------------------------------------
+ * fa_bwd_noalloc -- fa_bwd for callers that cannot allocate device memory.
+ * The FlashAttention pages have no counterpart; this is an interface
+ * convenience around the same backward kernels.
+ * Some callers cannot hand fa_bwd a workspace: code running inside a memory
+ * pool it does not own, hooks where allocation is forbidden, or plain C
+ * programs without a device allocator.  This entry point takes the
+ * backward pass's scratch (dQ accumulator, padded LSE / D rows, status word)
+ * from a fixed 64 MiB array compiled into the library's device image; every
+ * device that loads the library holds that array until the process exits.
+ * Arguments are those of fa_bwd without ws / ws_bytes.
+ *   - Returns FA_ERR_WORKSPACE, enqueuing nothing, when
+ *     fa_bwd_workspace_size(p) exceeds 64 MiB (roughly B*H*N > 240,000 rows
+ *     for 16-bit inputs).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the array and leave their contents in it;
+ *     what must start at zero is cleared on the stream by each call, but
+ *     calls whose GPU work overlaps (unordered streams) race on it.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ * fa_check_status cannot be used with it (there is no caller workspace).
+ * ------------------------------------------------------------------------- */
+fa_status fa_bwd_noalloc(const fa_params *p, const void *q, const void *k, const void *v,
+                         const void *o, const void *dout, const float *lse,
+                         void *dq, void *dk, void *dv, void *stream);
+
+/* ---------------------------------------------------------------------------
  * fa_check_status -- synchronises `stream`, then reads the status word the
  * last fa_fwd/fa_bwd on `ws` left: FA_OK, or FA_ERR_TIMEOUT if a bounded
  * device wait ran out (outputs are then undefined).  FA_ERR_CUDA if the
