@@ -174,11 +174,6 @@ struct ProfScope {
   }
 };
 
-bool fwd_p_in_tmem() {
-  const char* v = std::getenv("FA_FWD_P_SMEM");
-  return !(v != nullptr && v[0] == '1');
-}
-
 }  // namespace
 }  // namespace fa
 
@@ -230,7 +225,7 @@ fa_status fa_fwd(const fa_params* p, const void* q, const void* k, const void* v
       (s = map16(&mv, v, p, sd)) != FA_OK || (s = map16(&mo, o, p, sd)) != FA_OK)
     return s;
   ProfScope prof(p, st);
-  return cuda_status(launch_fwd_tc(p->dtype, fwd_p_in_tmem(), mq, mk, mv, mo, a, st));
+  return cuda_status(launch_fwd_tc(p->dtype, mq, mk, mv, mo, a, st));
 }
 
 fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v, const void* o, const void* dout,

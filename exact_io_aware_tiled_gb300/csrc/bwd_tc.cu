@@ -12,36 +12,44 @@
 //     dV += P~^T dO_i,  dK += dS^T Q_i,  dQ_i += dS K      (tau applied at the end)
 //
 // GB300 mapping (ours): one CTA per (b, h, 128-key tile), looping over the
-// query tiles that see it (causal / sparse lists).
+// query tiles that see it; the CTAs of one head are adjacent in launch order
+// so its Q / dO tiles and dQ accumulator rows stay in L2.
 //   * warp 8: TMA loads of K, V once and of Q_i, dO_i (+ LSE_i, D_i rows) into
 //     a two-stage ring;
-//   * warp 9: tcgen05 MMAs; S^T and dP^T go to tensor memory, dK and dV
-//     accumulate in tensor memory for the whole loop, dQ_i goes to tensor
-//     memory per step;
-//   * warps 0-3: one thread per key row: P^T, dS^T in registers, written as
-//     16-bit swizzled tiles to shared memory (they feed dV, dK as K-major A
-//     operands and dQ as an MN-major A operand);
-//   * warps 4-7: one thread per query row: read dQ_i from tensor memory,
-//     scale by tau, stage in shared memory, TMA reduce-add into a float32
-//     accumulator in global memory.
-// Tensor memory: S^T 0-127 | dP^T 128-255 | dK 256-319 | dV 320-383 | dQ 384-447.
+//   * warp 9: one thread issues the tcgen05 MMAs in the order
+//       dV(i) | S(i+1) | dK(i) | dP(i+1) | dQ(i)
+//     so the next step's S^T and dP^T are computed while the softmax warps
+//     still work on step i;
+//   * warps 0-3 / 4-7: two warpgroups, each owning 64 of the 128 query
+//     columns of every key row (= tensor-memory lane):
+//       part 1: P from S^T, P~^T (16 bit) into tensor memory for dV;
+//       part 2: dS from dP^T, dS^T (16 bit) into tensor memory for dK (each
+//               warpgroup overwrites only the dP^T columns it read itself)
+//               and into a swizzled shared tile for dQ;
+//       drain:  dQ_i from tensor memory -> x tau -> double-buffered shared
+//               staging;
+//   * warp 10: one thread turns each filled staging buffer into two TMA
+//     reduce-adds into the float32 dQ accumulator.
+// Tensor memory (512 columns):
+//   S^T 0-127 | dP^T 128-255 (dS^T, 16 bit: queries 0-63 at 128-159,
+//   64-127 at 192-223) | dK 256-319 | dV 320-383 | dQ 384-447 |
+//   P~^T (16 bit) 448-511.
 #include "common.cuh"
 
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int NSB = 2;   // Q / dO stages
 
 struct BwdSmem {
   static constexpr int kK = 0;
   static constexpr int kV = 16384;
-  static constexpr int kQ = 32768;              // NSB x 16 KB
-  static constexpr int kDO = kQ + NSB * 16384;  // NSB x 16 KB
-  static constexpr int kPT = kDO + NSB * 16384; // 32 KB: P~^T [2 chunks][128 keys][64 q]
-  static constexpr int kDS = kPT + 32768;       // 32 KB: dS^T, same layout
-  static constexpr int kDQ = kDS + 32768;       // 32 KB: float32 dQ staging [2][128][32]
-  static constexpr int kLD = kDQ + 32768;       // NSB x (LSE2[128] + D[128]) floats
+  static constexpr int kQ = 32768;                  // NSB x 16 KB
+  static constexpr int kDO = kQ + NSB * 16384;      // NSB x 16 KB
+  static constexpr int kDS = kDO + NSB * 16384;     // 32 KB: dS^T [2 chunks][128 keys][64 q]
+  static constexpr int kDQ = kDS + 32768;           // 2 x 32 KB: float32 dQ staging [buf][half][128][32]
+  static constexpr int kLD = kDQ + 65536;           // NSB x (LSE2[128] + D[128]) floats
   static constexpr int kBar = kLD + NSB * 1024;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kDyn = kBytes + 1024;
@@ -50,7 +58,9 @@ struct BwdSmem {
 struct BBars {
   uint64_t kv_full;
   uint64_t q_full[NSB], q_empty[NSB];
-  uint64_t st_full, ds_full, pds_free, dq_full, dq_free, dkv_full, mma_done;
+  uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free, dkv_full, mma_done;
+  uint64_t dsm_free;
+  uint64_t stg_full[2], stg_free[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -67,6 +77,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
+constexpr uint32_t kColST = 0, kColDP = 128, kColDK = 256, kColDV = 320, kColDQ = 384, kColPT = 448;
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -80,10 +92,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item: (b, h, key tile jt); for causal the longest lists first
-  const int BH = a.B * a.H;
-  const int jt = (int)(blockIdx.x / BH);
-  const int bh = (int)(blockIdx.x % BH);
+  // ---- work item: (b, h, key tile jt); the tiles of one head are adjacent,
+  //      and under causal masking the longest query lists come first.
+  const int bh = (int)(blockIdx.x / a.nq);
+  const int jt = (int)(blockIdx.x % a.nq);
   const int b = bh / a.H, h = bh % a.H;
   int Lk = a.N;
   if (a.mask.seqlens_k != nullptr) Lk = max(0, min(a.N, a.mask.seqlens_k[b]));
@@ -112,13 +124,19 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1);
     }
-    mbar_init(&bars->st_full, 1);
-    mbar_init(&bars->ds_full, 128);
-    mbar_init(&bars->pds_free, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->dq_free, 256);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->dsm_free, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->stg_full[i], 256);
+      mbar_init(&bars->stg_free[i], 1);
+    }
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -161,170 +179,283 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // ===================== MMA issuer =====================
     if (lane == 0 && n > 0) {
       constexpr int ab = Cvt<T>::kAB;
-      constexpr uint32_t idST = idesc_f16(128, 128, ab, 0, 0);   // S^T, dP^T
-      constexpr uint32_t idKV = idesc_f16(128, 64, ab, 0, 1);    // dV, dK (A K-major, B MN-major)
+      constexpr uint32_t idST = idesc_f16(128, 128, ab, 0, 0);   // S^T, dP^T (both operands K-major)
+      constexpr uint32_t idKV = idesc_f16(128, 64, ab, 0, 1);    // dV, dK (A from tensor memory, B MN-major)
       constexpr uint32_t idQ = idesc_f16(128, 64, ab, 1, 1);     // dQ (A MN-major, B MN-major)
       const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
       const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
-      const uint32_t sPT = smem_u32(smem + L::kPT), sDS = smem_u32(smem + L::kDS);
-      const uint32_t tST = tmem, tDP = tmem + 128, tDK = tmem + 256, tDV = tmem + 320, tDQ = tmem + 384;
+      const uint32_t sDS = smem_u32(smem + L::kDS);
+      auto issue_st = [&](int st1) {   // S^T = K Q^T
+        const uint32_t q1 = sQ + st1 * 16384;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tmem + kColST, sdesc_sw128(sK + k * 32, 16, 1024), sdesc_sw128(q1 + k * 32, 16, 1024), idST,
+                 k > 0 ? 1u : 0u);
+      };
+      auto issue_dp = [&](int st1) {   // dP^T = V dO^T
+        const uint32_t d1 = sDO + st1 * 16384;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tmem + kColDP, sdesc_sw128(sV + k * 32, 16, 1024), sdesc_sw128(d1 + k * 32, 16, 1024), idST,
+                 k > 0 ? 1u : 0u);
+      };
       bool ok = mbar_wait(&bars->kv_full, 0, ctl) && mbar_wait(&bars->q_full[0], 0, ctl);
       if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tST, sdesc_sw128(sK + k * 32, 16, 1024), sdesc_sw128(sQ + k * 32, 16, 1024), idST, k > 0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tDP, sdesc_sw128(sV + k * 32, 16, 1024), sdesc_sw128(sDO + k * 32, 16, 1024), idST, k > 0);
-        mma_commit(&bars->st_full);
+        issue_st(0);
+        mma_commit(&bars->s_full);
+        issue_dp(0);
+        mma_commit(&bars->dp_full);
       }
       for (int t = 0; t < n && ok; ++t) {
         const int st = t % NSB;
-        if (!(ok = mbar_wait(&bars->ds_full, (uint32_t)t & 1u, ctl))) break;
+        const uint32_t qb = sQ + st * 16384, db = sDO + st * 16384;
+        const bool more = t + 1 < n;
+        const int st1 = (t + 1) % NSB;
+        // dV += P~^T dO_t  (A = P~^T in tensor memory; K-dim = 128 queries, 8 steps of 16)
+        if (!(ok = mbar_wait(&bars->p_full, (uint32_t)t & 1u, ctl))) break;
         tc_fence_after();
-        if (t + 1 < n) {
-          const int st1 = (t + 1) % NSB;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tmem + kColDV, tmem + kColPT + k * 8, sdesc_sw128(db + k * 2048, 16384, 1024), idKV,
+                 (t > 0 || k > 0) ? 1u : 0u);
+        // S^T(t+1): its columns were consumed by part 1 of step t
+        if (more) {
           if (!(ok = mbar_wait(&bars->q_full[st1], (uint32_t)((t + 1) / NSB) & 1u, ctl))) break;
           tc_fence_after();
-          const uint32_t q1 = sQ + st1 * 16384, d1 = sDO + st1 * 16384;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tST, sdesc_sw128(sK + k * 32, 16, 1024), sdesc_sw128(q1 + k * 32, 16, 1024), idST, k > 0);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tDP, sdesc_sw128(sV + k * 32, 16, 1024), sdesc_sw128(d1 + k * 32, 16, 1024), idST, k > 0);
-          mma_commit(&bars->st_full);
+          issue_st(st1);
+          mma_commit(&bars->s_full);
         }
-        const uint32_t qb = sQ + st * 16384, db = sDO + st * 16384;
-        // dV += P~^T dO_i ; dK += dS^T Q_i   (K-dim = 128 queries, 8 steps of 16)
+        // dK += dS^T Q_t  (A = dS^T in tensor memory)
+        if (!(ok = mbar_wait(&bars->ds_full, (uint32_t)t & 1u, ctl))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t aoff = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tDV, sdesc_sw128(sPT + aoff, 16, 1024), sdesc_sw128(db + k * 2048, 16384, 1024), idKV,
-                 (t > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tmem + kColDK, tmem + kColDP + (k >> 2) * 64 + (k & 3) * 8, sdesc_sw128(qb + k * 2048, 16384, 1024),
+                 idKV, (t > 0 || k > 0) ? 1u : 0u);
+        // dP^T(t+1): overwrites dS^T(t), which dK(t) above has read (MMAs run in issue order)
+        if (more) {
+          issue_dp(st1);
+          mma_commit(&bars->dp_full);
         }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t aoff = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tDK, sdesc_sw128(sDS + aoff, 16, 1024), sdesc_sw128(qb + k * 2048, 16384, 1024), idKV,
-                 (t > 0 || k > 0) ? 1u : 0u);
-        }
-        // dQ_i = dS K  (M = 128 queries, K-dim = 128 keys)
+        // dQ_t = dS K  (M = 128 queries from the MN-major view of dS^T, K-dim = 128 keys)
         if (t > 0 && !(ok = mbar_wait(&bars->dq_free, (uint32_t)(t - 1) & 1u, ctl))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ss(tDQ, sdesc_sw128(sDS + k * 2048, 16384, 1024), sdesc_sw128(sK + k * 2048, 16384, 1024), idQ,
-                 k > 0 ? 1u : 0u);
+          mma_ss(tmem + kColDQ, sdesc_sw128(sDS + k * 2048, 16384, 1024), sdesc_sw128(sK + k * 2048, 16384, 1024),
+                 idQ, k > 0 ? 1u : 0u);
         mma_commit(&bars->dq_full);
-        mma_commit(&bars->pds_free);
+        mma_commit(&bars->dsm_free);
         mma_commit(&bars->q_empty[st]);
       }
       mma_commit(&bars->dkv_full);
       mma_commit(&bars->mma_done);
       mbar_wait(&bars->mma_done, 0, ctl);
     }
-  } else if (warp < 4) {
-    // ===================== P^T / dS^T (one thread per key) =====================
-    const int r = warp * 32 + lane;
-    const int j = jt * kTile + r;                     // global key
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t tST = tmem + lane_off, tDP = tST + 128;
+  } else if (warp == 10) {
+    // ===================== dQ reduce issuer =====================
+    if (lane == 0 && n > 0) {
+      prefetch_tmap(&tmDQ);
+      for (int t = 0; t < n; ++t) {
+        const int bi = t & 1;
+        if (!mbar_wait(&bars->stg_full[bi], (uint32_t)(t >> 1) & 1u, ctl)) break;
+        const uint8_t* sb = smem + L::kDQ + bi * 32768;
+        const int qi = ql.qt(t);
+        tma_reduce_add_4d(&tmDQ, sb, 0, qi * kTile, h, b);
+        tma_reduce_add_4d(&tmDQ, sb + 16384, 32, qi * kTile, h, b);
+        bulk_commit();
+        bulk_wait_read0();
+        mbar_arrive(&bars->stg_free[bi]);
+      }
+      bulk_wait0();
+    }
+  } else if (warp < 8) {
+    // ===================== softmax-gradient warpgroups =====================
+    const int wg = warp >> 2;                 // 0: query columns 0-63, 1: 64-127
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;        // key row within the tile = TMEM lane
+    const int j = jt * kTile + r;             // global key
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tl = tmem + lane_off;
     const bool key_ok = j < Lk;
     const float sl2 = a.scale_log2;
     const uint32_t bh_rows = (uint32_t)bh * (uint32_t)a.N;
+    const int c0 = wg * 64;                   // first query column of this warpgroup
     bool ok = true;
+
+    // dQ_t: tensor memory -> x tau -> staging buffer t % 2 (warp 10 reduces it)
+    auto drain_dq = [&](int t) -> bool {
+      if (!warp_wait(&bars->dq_full, (uint32_t)t & 1u, ctl)) return false;
+      tc_fence_after();
+      uint32_t g[32];
+      tmem_ld32(tl + kColDQ + wg * 32, g);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);
+      const int bi = t & 1;
+      if (t >= 2 && !warp_wait(&bars->stg_free[bi], (uint32_t)((t - 2) >> 1) & 1u, ctl)) return false;
+      uint8_t* sb = smem + L::kDQ + bi * 32768 + wg * 16384 + r * 128;
+#pragma unroll
+      for (int pc = 0; pc < 8; ++pc) {
+        const uint32_t off = (((pc ^ r) & 7) << 4);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(smem_u32(sb + off)),
+                        "f"(__uint_as_float(g[pc * 4]) * a.scale), "f"(__uint_as_float(g[pc * 4 + 1]) * a.scale),
+                        "f"(__uint_as_float(g[pc * 4 + 2]) * a.scale), "f"(__uint_as_float(g[pc * 4 + 3]) * a.scale)
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->stg_full[bi]);
+      return true;
+    };
+
     for (int t = 0; t < n && ok; ++t) {
       const int st = t % NSB;
       const int qi = ql.qt(t);
-      if (!(ok = warp_wait(&bars->st_full, (uint32_t)t & 1u, ctl) &&
+      // LSE*log2e and D of this warpgroup's 64 query columns, in shared memory
+      const uint32_t s_lse = smem_u32(smem + L::kLD + st * 1024) + c0 * 4;
+      const uint32_t s_d = s_lse + 512;
+      // query column c (relative to c0) is hidden from this key under causal iff c0 + c < qlo
+      const int qlo = a.mask.causal ? (j - qi * kTile) : -1;
+      const bool any_mask = !key_ok || qlo > c0;
+
+      // ---- part 1: P from S^T
+      if (!(ok = warp_wait(&bars->s_full, (uint32_t)t & 1u, ctl) &&
                  warp_wait(&bars->q_full[st], (uint32_t)(t / NSB) & 1u, ctl))) break;
       tc_fence_after();
-      if (t > 0 && !(ok = warp_wait(&bars->pds_free, (uint32_t)(t - 1) & 1u, ctl))) break;
-      const float* lse2 = reinterpret_cast<const float*>(smem + L::kLD + st * 1024);
-      const float* dvec = lse2 + 128;
-      uint8_t* pt = smem + L::kPT;
-      uint8_t* ds = smem + L::kDS;
-      // last query (relative to the tile) that this key is hidden from under causal: q < j
-      const int qlo = a.mask.causal ? (j - qi * kTile) : -1;   // columns c < qlo... masked when c < qlo
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tST + cc * 32, sv);
-        tmem_ld32(tDP + cc * 32, dv);
-        tmem_wait_ld();
-        uint32_t keep = ~0u;
-        if (a.drop.enabled) {
-          keep = 0;
+      uint32_t sv[2][32];
+      tmem_ld32(tl + kColST + c0, sv[0]);
+      tmem_ld32(tl + kColST + c0 + 32, sv[1]);
+      uint32_t keep[2] = {~0u, ~0u};
+      if (a.drop.enabled) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t kb = 0;
 #pragma unroll 4
           for (int c = 0; c < 32; ++c) {
-            const uint32_t q = (uint32_t)(qi * kTile + cc * 32 + c);
+            const uint32_t q = (uint32_t)(qi * kTile + c0 + hf * 32 + c);
             const uint32_t bits = dropout_keep8((uint32_t)j >> 3, bh_rows + q, a.drop);
-            keep |= ((bits >> (j & 7)) & 1u) << c;
+            kb |= ((bits >> (j & 7)) & 1u) << c;
           }
-        }
-        uint32_t pw[16], dw[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float p[2], d[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cq = cc * 32 + c + e;
-            float pv = ex2(fmaf(__uint_as_float(sv[c + e]), sl2, -lse2[cq]));
-            if (!key_ok || cq < qlo) pv = 0.f;
-            const bool kept = (keep >> (c + e)) & 1u;
-            const float dpv = kept ? __uint_as_float(dv[c + e]) * a.drop.rp : 0.f;
-            p[e] = kept ? pv * a.drop.rp : 0.f;
-            d[e] = pv * (dpv - dvec[cq]);
-          }
-          pw[c >> 1] = Cvt<T>::pack(p[0], p[1]);
-          dw[c >> 1] = Cvt<T>::pack(d[0], d[1]);
-        }
-        // columns cc*32 .. +31 -> chunk cc/2, 16-byte pieces (cc&1)*4 .. +3
-        const uint32_t base = (cc >> 1) * 16384 + r * 128;
-#pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
-          const uint32_t piece = (cc & 1) * 4 + pc;
-          const uint32_t off = base + (((piece ^ (uint32_t)r) & 7u) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                       :: "r"(smem_u32(pt + off)), "r"(pw[pc * 4]), "r"(pw[pc * 4 + 1]), "r"(pw[pc * 4 + 2]),
-                          "r"(pw[pc * 4 + 3]) : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                       :: "r"(smem_u32(ds + off)), "r"(dw[pc * 4]), "r"(dw[pc * 4 + 1]), "r"(dw[pc * 4 + 2]),
-                          "r"(dw[pc * 4 + 3]) : "memory");
+          keep[hf] = kb;
         }
       }
+      tmem_wait_ld();
+      uint32_t pp[32];      // undropped P, 16 bit, kept for part 2
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pt[16];    // P~ = Z o P / (1 - p), 16 bit, operand of dV
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 l4 = lds128(s_lse + (hf * 32 + q4 * 4) * 4);
+          float x[4];
+          fma2(x[0], x[1], __uint_as_float(sv[hf][q4 * 4]), __uint_as_float(sv[hf][q4 * 4 + 1]), sl2, sl2, -l4.x, -l4.y);
+          fma2(x[2], x[3], __uint_as_float(sv[hf][q4 * 4 + 2]), __uint_as_float(sv[hf][q4 * 4 + 3]), sl2, sl2, -l4.z, -l4.w);
+          float p[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) p[e] = ex2(x[e]);
+          if (any_mask) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (!key_ok || c0 + hf * 32 + q4 * 4 + e < qlo) p[e] = 0.f;
+          }
+          const uint32_t w0 = Cvt<T>::pack(p[0], p[1]), w1 = Cvt<T>::pack(p[2], p[3]);
+          pp[hf * 16 + q4 * 2] = w0;
+          pp[hf * 16 + q4 * 2 + 1] = w1;
+          if (a.drop.enabled) {
+            const uint32_t kb = keep[hf] >> (q4 * 4);
+            const float rp = a.drop.rp;
+            pt[q4 * 2] = Cvt<T>::pack((kb & 1u) ? p[0] * rp : 0.f, (kb & 2u) ? p[1] * rp : 0.f);
+            pt[q4 * 2 + 1] = Cvt<T>::pack((kb & 4u) ? p[2] * rp : 0.f, (kb & 8u) ? p[3] * rp : 0.f);
+          } else {
+            pt[q4 * 2] = w0;
+            pt[q4 * 2 + 1] = w1;
+          }
+        }
+        tmem_st16(tl + kColPT + wg * 32 + hf * 16, pt);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+
+      // ---- part 2: dS from dP^T
+      if (!(ok = warp_wait(&bars->dp_full, (uint32_t)t & 1u, ctl))) break;
+      tc_fence_after();
+      uint32_t dv[2][32];
+      tmem_ld32(tl + kColDP + c0, dv[0]);
+      tmem_ld32(tl + kColDP + c0 + 32, dv[1]);
+      tmem_wait_ld();
+      // dS^T also goes to the shared tile, once dQ of the previous step has read it
+      if (t >= 1 && !(ok = warp_wait(&bars->dsm_free, (uint32_t)(t - 1) & 1u, ctl))) break;
+      uint8_t* dsb = smem + L::kDS + wg * 16384 + r * 128;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t dsw[16];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 d4 = lds128(s_d + (hf * 32 + q4 * 4) * 4);
+          float g[4] = {__uint_as_float(dv[hf][q4 * 4]), __uint_as_float(dv[hf][q4 * 4 + 1]),
+                        __uint_as_float(dv[hf][q4 * 4 + 2]), __uint_as_float(dv[hf][q4 * 4 + 3])};
+          if (a.drop.enabled) {
+            const uint32_t kb = keep[hf] >> (q4 * 4);
+            const float rp = a.drop.rp;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) g[e] = ((kb >> e) & 1u) ? g[e] * rp : 0.f;
+          }
+          const uint32_t w0 = pp[hf * 16 + q4 * 2], w1 = pp[hf * 16 + q4 * 2 + 1];
+          float y[4];
+          sub2(y[0], y[1], g[0], g[1], d4.x, d4.y);
+          sub2(y[2], y[3], g[2], g[3], d4.z, d4.w);
+          mul2(y[0], y[1], y[0], y[1], Cvt<T>::lo(w0), Cvt<T>::hi(w0));
+          mul2(y[2], y[3], y[2], y[3], Cvt<T>::lo(w1), Cvt<T>::hi(w1));
+          dsw[q4 * 2] = Cvt<T>::pack(y[0], y[1]);
+          dsw[q4 * 2 + 1] = Cvt<T>::pack(y[2], y[3]);
+        }
+        tmem_st16(tl + kColDP + c0 + hf * 16, dsw);   // inside this warpgroup's own dP^T columns
+#pragma unroll
+        for (int pc4 = 0; pc4 < 4; ++pc4) {
+          const int pc = hf * 4 + pc4;
+          const uint32_t off = (((pc ^ r) & 7) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                       :: "r"(smem_u32(dsb + off)), "r"(dsw[pc4 * 4]), "r"(dsw[pc4 * 4 + 1]), "r"(dsw[pc4 * 4 + 2]),
+                          "r"(dsw[pc4 * 4 + 3]) : "memory");
+        }
+      }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->ds_full);
+
+      // ---- drain dQ of the previous step
+      if (t > 0 && !(ok = drain_dq(t - 1))) break;
     }
+    if (ok && n > 0) ok = drain_dq(n - 1);
+
     // ---- epilogue: dK (x tau), dV -> 16 bit -> shared -> TMA store
-    named_bar_sync(1, 128);
-    if (!bars->abort) {
-      uint32_t kraw[2][32], vraw[2][32];
+    if (!named_bar_or(1, 256, !ok || bars->abort)) {
+      uint32_t kraw[32], vraw[32];
       bool have = false;
       if (n > 0 && warp_wait(&bars->dkv_full, 0, ctl)) {
         tc_fence_after();
-        tmem_ld32(tmem + lane_off + 256, kraw[0]);
-        tmem_ld32(tmem + lane_off + 288, kraw[1]);
-        tmem_ld32(tmem + lane_off + 320, vraw[0]);
-        tmem_ld32(tmem + lane_off + 352, vraw[1]);
+        tmem_ld32(tl + kColDK + wg * 32, kraw);
+        tmem_ld32(tl + kColDV + wg * 32, vraw);
         tmem_wait_ld();
         have = true;
       }
-      uint8_t* kb = smem + L::kPT;          // P^T / dS^T are dead after dkv_full
-      uint8_t* vb = smem + L::kPT + 16384;
+      uint8_t* kb = smem + L::kDS;          // dS^T buffers are dead after dkv_full
+      uint8_t* vb = smem + L::kDS + 16384;
 #pragma unroll
-      for (int pc = 0; pc < 8; ++pc) {
+      for (int pc4 = 0; pc4 < 4; ++pc4) {
+        const int pc = wg * 4 + pc4;        // 16-byte piece = 8 columns
         uint32_t wk[4], wv[4];
 #pragma unroll
         for (int t2 = 0; t2 < 4; ++t2) {
-          const int c = pc * 8 + 2 * t2;
-          const float k0 = have ? __uint_as_float(kraw[c >> 5][c & 31]) * a.scale : 0.f;
-          const float k1 = have ? __uint_as_float(kraw[(c + 1) >> 5][(c + 1) & 31]) * a.scale : 0.f;
-          const float v0 = have ? __uint_as_float(vraw[c >> 5][c & 31]) : 0.f;
-          const float v1 = have ? __uint_as_float(vraw[(c + 1) >> 5][(c + 1) & 31]) : 0.f;
+          const int c = pc4 * 8 + 2 * t2;   // column within this warpgroup's 32
+          const float k0 = have ? __uint_as_float(kraw[c]) * a.scale : 0.f;
+          const float k1 = have ? __uint_as_float(kraw[c + 1]) * a.scale : 0.f;
+          const float v0 = have ? __uint_as_float(vraw[c]) : 0.f;
+          const float v1 = have ? __uint_as_float(vraw[c + 1]) : 0.f;
           wk[t2] = Cvt<T>::pack(k0, k1);
           wv[t2] = Cvt<T>::pack(v0, v1);
         }
@@ -335,54 +466,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                      :: "r"(smem_u32(vb + off)), "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3]) : "memory");
       }
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (r == 0) {
+      named_bar_sync(1, 256);
+      if (threadIdx.x == 0) {
         tma_store_4d(&tmDK, kb, 0, jt * kTile, h, b);
         tma_store_4d(&tmDV, vb, 0, jt * kTile, h, b);
         bulk_commit();
         bulk_wait0();
       }
     }
-  } else {
-    // ===================== dQ: one thread per query row =====================
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const uint32_t tDQ = tmem + ((uint32_t)(quarter * 32) << 16) + 384;
-    float* stg = reinterpret_cast<float*>(smem + L::kDQ);
-    bool ok = true;
-    for (int t = 0; t < n && ok; ++t) {
-      const int qi = ql.qt(t);
-      if (!(ok = warp_wait(&bars->dq_full, (uint32_t)t & 1u, ctl))) break;
-      tc_fence_after();
-      uint32_t g[2][32];
-      tmem_ld32(tDQ, g[0]);
-      tmem_ld32(tDQ + 32, g[1]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars->dq_free);
-      // the previous reduce must have finished reading the staging buffer
-      if (r == 0) bulk_wait_read0();
-      named_bar_sync(2, 128);
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int pc = 0; pc < 8; ++pc) {
-          const uint32_t off = hf * 16384 + r * 128 + (((pc ^ r) & 7) << 4);
-          const float* gv = reinterpret_cast<const float*>(&g[hf][pc * 4]);
-          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
-                       :: "r"(smem_u32(reinterpret_cast<uint8_t*>(stg) + off)),
-                          "f"(gv[0] * a.scale), "f"(gv[1] * a.scale), "f"(gv[2] * a.scale), "f"(gv[3] * a.scale)
-                       : "memory");
-        }
-      fence_proxy_async_smem();
-      named_bar_sync(2, 128);
-      if (r == 0) {
-        tma_reduce_add_4d(&tmDQ, stg, 0, qi * kTile, h, b);
-        tma_reduce_add_4d(&tmDQ, reinterpret_cast<uint8_t*>(stg) + 16384, 32, qi * kTile, h, b);
-        bulk_commit();
-      }
-    }
-    if (r == 0) bulk_wait0();
   }
 
   tc_fence_before();

@@ -5,7 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/fa.h"
+#include "fa.h"
 
 namespace fa {
 
@@ -61,8 +61,8 @@ struct BwdArgs {
 // ---------------------------------------------------------------------------
 // Launchers (defined in the .cu files; all enqueue on `stream`).
 // ---------------------------------------------------------------------------
-cudaError_t launch_fwd_tc(int dtype, bool p_in_tmem, const CUtensorMap& q, const CUtensorMap& k,
-                          const CUtensorMap& v, const CUtensorMap& o, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_fwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const CUtensorMap& o, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
                           const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s);

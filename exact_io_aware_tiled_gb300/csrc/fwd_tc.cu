@@ -14,11 +14,16 @@
 //   * warp 8 (one thread) streams K/V tiles with TMA into a ring of NS
 //     stages; a stage is shared by both slots when both need the same KV tile
 //     at the same step;
-//   * warp 9 (one thread) issues tcgen05 MMAs: S_x = Q_x K^T into tensor
-//     memory, then O_x += P_x V with P_x read from tensor memory (or, in the
-//     alternative build, from shared memory);
+//   * tcgen05 MMAs are issued by three warps, because one issuing thread
+//     sustains only about one MMA per ~100 cycles whatever its size:
+//       warp 9  issues S_x = Q_x K^T for both slots, as soon as the softmax
+//               has copied the previous S_x into registers;
+//       warp 10 / 11 issue O_x += P_x V for slot 0 / 1 (P_x from tensor
+//               memory);
 //   * warps 0-3 / 4-7 run the softmax of slot 0 / 1, one thread per query
-//     row (= tensor-memory lane): max, exp2, row sums, dropout, P in 16 bit;
+//     row (= tensor-memory lane).  P is computed into registers while the
+//     previous PV MMA still runs; only the O rescale and the P store wait
+//     for it;
 //   * O is rescaled only when the running row max grows by more than 2^8
 //     (the final O / l and the logsumexp use the same reference max, so the
 //     result is unchanged); O is normalised by the sum of the rounded P that
@@ -31,26 +36,25 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr int NS = 5;                       // K/V stages
 
-template <bool kPTmem> struct FwdCfg {
-  static constexpr int NS = kPTmem ? 5 : 3;              // K/V stages
+struct FwdCfg {
   static constexpr int kQ = 0;                           // 2 x 16 KB
   static constexpr int kK = 32768;                       // NS x 16 KB
   static constexpr int kV = kK + NS * 16384;             // NS x 16 KB
-  static constexpr int kP = kV + NS * 16384;             // 2 x 32 KB (shared-memory P only)
-  static constexpr int kBar = kP + (kPTmem ? 0 : 65536);
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kBar = kV + NS * 16384;
+  static constexpr int kBytes = kBar + 512;
   static constexpr int kDyn = kBytes + 1024;             // + alignment slack
 };
 
 struct Bars {
   uint64_t q_full;
-  uint64_t s_full[2], p_full[2], o_full[2];
-  uint64_t mma_done;
-  uint64_t k_full[5], v_full[5], kv_empty[5];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t done[3];
+  uint64_t k_full[NS], v_full[NS], k_empty[NS], v_empty[NS];
   uint32_t tmem_base;
   int abort;
 };
@@ -82,18 +86,49 @@ __device__ __forceinline__ Slot make_slot(const FwdArgs& a, int qt, int Lk) {
   return sl;
 }
 
+// The K/V tiles loaded at one step: one stage when both slots need the same
+// tile (or only one slot has a step), two otherwise.  Every role walks the
+// same sequence, so all agree on stage indices and phases.
+struct StepPlan {
+  int nl;                 // loads at this step (0..2)
+  int st[2];              // stage of each load
+  uint32_t ph[2];         // phase parity of each load
+  int kv[2];              // kv tile of each load
+  int use[2];             // load index used by slot x, or -1
+};
+
+__device__ __forceinline__ StepPlan plan_step(const Slot (&sl)[2], int s, int& ld) {
+  StepPlan p;
+  p.nl = 0;
+  p.use[0] = p.use[1] = -1;
+  const int kvA = s < sl[0].n ? sl[0].kv(s) : -1;
+  const int kvB = s < sl[1].n ? sl[1].kv(s) : -1;
+  if (kvA >= 0) {
+    p.st[0] = ld % NS; p.ph[0] = (uint32_t)(ld / NS) & 1u; p.kv[0] = kvA; ++ld;
+    p.use[0] = 0; p.nl = 1;
+  }
+  if (kvB >= 0) {
+    if (kvB == kvA) {
+      p.use[1] = 0;
+    } else {
+      p.st[p.nl] = ld % NS; p.ph[p.nl] = (uint32_t)(ld / NS) & 1u; p.kv[p.nl] = kvB; ++ld;
+      p.use[1] = p.nl; ++p.nl;
+    }
+  }
+  return p;
+}
+
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
   const bool ok = mbar_wait(bar, parity, ctl);
   return __all_sync(0xffffffffu, ok);
 }
 
-template <typename T, bool kPTmem>
+template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
               const FwdArgs a) {
-  using C = FwdCfg<kPTmem>;
-  constexpr int NS = C::NS;
+  using C = FwdCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kBar);
@@ -119,14 +154,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(&bars->q_full, 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars->s_full[x], 1);
+      mbar_init(&bars->s_free[x], 128);
       mbar_init(&bars->p_full[x], 128);
-      mbar_init(&bars->o_full[x], 1);
+      mbar_init(&bars->pv_done[x], 1);
     }
-    mbar_init(&bars->mma_done, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&bars->done[i], 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_empty[s], 2);
     }
     bars->abort = 0;
     fence_mbar_init();
@@ -139,6 +176,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  constexpr int ab = Cvt<T>::kAB;
 
   if (warp == 8) {
     // ===================== TMA producer =====================
@@ -155,19 +193,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       int ld = 0;
       bool ok = true;
       for (int s = 0; s < smax && ok; ++s) {
-        const int kvA = s < sl[0].n ? sl[0].kv(s) : -1;
-        const int kvB = s < sl[1].n ? sl[1].kv(s) : -1;
-        int todo[2] = {kvA, (kvB >= 0 && kvB != kvA) ? kvB : -1};
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (todo[t] < 0) continue;
-          const int st = ld % NS;
-          const uint32_t ph = (uint32_t)(ld / NS) & 1u;
-          ++ld;
-          if (!mbar_wait(&bars->kv_empty[st], ph ^ 1u, ctl)) { ok = false; break; }
+        const StepPlan p = plan_step(sl, s, ld);
+        for (int l = 0; l < p.nl; ++l) {
+          const int st = p.st[l];
+          if (!(ok = mbar_wait(&bars->k_empty[st], p.ph[l] ^ 1u, ctl) &&
+                     mbar_wait(&bars->v_empty[st], p.ph[l] ^ 1u, ctl)))
+            break;
           mbar_expect_tx(&bars->k_full[st], 16384);
-          tma_load_4d(smem + C::kK + st * 16384, &tmK, &bars->k_full[st], 0, todo[t] * kTile, h, b);
+          tma_load_4d(smem + C::kK + st * 16384, &tmK, &bars->k_full[st], 0, p.kv[l] * kTile, h, b);
           mbar_expect_tx(&bars->v_full[st], 16384);
-          tma_load_4d(smem + C::kV + st * 16384, &tmV, &bars->v_full[st], 0, todo[t] * kTile, h, b);
+          tma_load_4d(smem + C::kV + st * 16384, &tmV, &bars->v_full[st], 0, p.kv[l] * kTile, h, b);
         }
       }
       // Before leaving, make sure no load is still writing shared memory.
@@ -178,76 +213,71 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (qbytes > 0) mbar_wait(&bars->q_full, 0, ctl);
     }
   } else if (warp == 9) {
-    // ===================== MMA issuer =====================
+    // ===================== S issuer (both slots) =====================
     if (lane == 0 && smax > 0) {
-      constexpr int ab = Cvt<T>::kAB;
       constexpr uint32_t idS = idesc_f16(128, 128, ab, 0, 0);
-      constexpr uint32_t idPV = idesc_f16(128, 64, ab, 0, 1);
-      const uint32_t sQ = smem_u32(smem + C::kQ), sK = smem_u32(smem + C::kK), sV = smem_u32(smem + C::kV);
-      const uint32_t sP = smem_u32(smem + C::kP);
+      const uint64_t qd[2] = {sdesc_sw128(smem_u32(smem + C::kQ), 16, 1024),
+                              sdesc_sw128(smem_u32(smem + C::kQ + 16384), 16, 1024)};
+      const uint64_t kd0 = sdesc_sw128(smem_u32(smem + C::kK), 16, 1024);
       bool ok = mbar_wait(&bars->q_full, 0, ctl);
       int ld = 0;
-      int pst[2] = {-1, -1};
-      uint32_t pph[2] = {0, 0};
-      bool pshared = false;   // both slots used one stage at the previous step
-      for (int s = 0; s <= smax && ok; ++s) {
-        int st[2] = {-1, -1};
-        uint32_t ph[2] = {0, 0};
-        bool shared = false;
-        if (s < smax) {
-          const int kvA = s < sl[0].n ? sl[0].kv(s) : -1;
-          const int kvB = s < sl[1].n ? sl[1].kv(s) : -1;
-          if (kvA >= 0) { st[0] = ld % NS; ph[0] = (uint32_t)(ld / NS) & 1u; ++ld; }
-          if (kvB >= 0) {
-            if (kvB == kvA) { st[1] = st[0]; ph[1] = ph[0]; shared = true; }
-            else { st[1] = ld % NS; ph[1] = (uint32_t)(ld / NS) & 1u; ++ld; }
-          }
-        }
+      for (int s = 0; s < smax && ok; ++s) {
+        const StepPlan p = plan_step(sl, s, ld);
         for (int x = 0; x < 2 && ok; ++x) {
-          const int n = sl[x].n;
-          if (n == 0 || s > n) continue;
-          const uint32_t tS = tmem + x * 256, tP = tS + 128, tO = tS + 192;
-          if (s > 0) {
-            // O_x += P_x(s-1) V(s-1)
-            ok = mbar_wait(&bars->p_full[x], (uint32_t)(s - 1) & 1u, ctl) &&
-                 mbar_wait(&bars->v_full[pst[x]], pph[x], ctl);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t vb = sV + pst[x] * 16384;
+          if (s >= sl[x].n) continue;
+          const int l = p.use[x];
+          if (s > 0 && !(ok = mbar_wait(&bars->s_free[x], (uint32_t)(s - 1) & 1u, ctl))) break;
+          if (!(ok = mbar_wait(&bars->k_full[p.st[l]], p.ph[l], ctl))) break;
+          tc_fence_after();
+          const uint64_t kd = kd0 + (uint64_t)((p.st[l] * 16384) >> 4);
+          const uint32_t tS = tmem + x * 256;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint64_t bd = sdesc_sw128(vb + k * 2048, 16384, 1024);
-              const uint32_t acc = (s > 1 || k > 0) ? 1u : 0u;
-              if constexpr (kPTmem) {
-                mma_ts(tO, tP + k * 8, bd, idPV, acc);
-              } else {
-                const uint64_t adsc = sdesc_sw128(sP + x * 32768 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-                mma_ss(tO, adsc, bd, idPV, acc);
-              }
-            }
-            // A stage both slots read is released after slot 1's PV.
-            if (!(pshared && x == 0)) mma_commit(&bars->kv_empty[pst[x]]);
-            if (s == n) mma_commit(&bars->o_full[x]);
-          }
-          if (s < n) {
-            // S_x(s) = Q_x K(s)^T
-            if (!(ok = mbar_wait(&bars->k_full[st[x]], ph[x], ctl))) break;
-            tc_fence_after();
-            const uint32_t qb = sQ + x * 16384, kb = sK + st[x] * 16384;
+          for (int k = 0; k < 4; ++k) mma_ss(tS, qd[x] + 2 * k, kd + 2 * k, idS, k > 0 ? 1u : 0u);
+          mma_commit(&bars->s_full[x]);
+        }
+        for (int l = 0; l < p.nl && ok; ++l) mma_commit(&bars->k_empty[p.st[l]]);
+      }
+      mma_commit(&bars->done[0]);
+      mbar_wait(&bars->done[0], 0, ctl);
+    }
+  } else if (warp >= 10) {
+    // ===================== PV issuer of slot x =====================
+    const int x = warp - 10;
+    if (lane == 0 && smax > 0) {
+      constexpr uint32_t idPV = idesc_f16(128, 64, ab, 0, 1);
+      const uint64_t vd0 = sdesc_sw128(smem_u32(smem + C::kV), 16384, 1024);
+      const uint32_t tP = tmem + x * 256 + 128, tO = tmem + x * 256 + 192;
+      const int n = sl[x].n;
+      int ld = 0;
+      bool ok = true;
+      for (int s = 0; s < smax && ok; ++s) {
+        const StepPlan p = plan_step(sl, s, ld);
+        if (s < n) {
+          const int l = p.use[x];
+          const int st = p.st[l];
+          if (!(ok = mbar_wait(&bars->p_full[x], (uint32_t)s & 1u, ctl) &&
+                     mbar_wait(&bars->v_full[st], p.ph[l], ctl)))
+            break;
+          tc_fence_after();
+          const uint64_t vd = vd0 + (uint64_t)((st * 16384) >> 4);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss(tS, sdesc_sw128(qb + k * 32, 16, 1024), sdesc_sw128(kb + k * 32, 16, 1024), idS,
-                     k > 0 ? 1u : 0u);
-            mma_commit(&bars->s_full[x]);
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tO, tP + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idPV, (s > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bars->pv_done[x]);
+        }
+        // one arrival per slot on every loaded stage: after our MMAs for a
+        // stage we read, right away (once it is loaded) for one we did not
+        for (int l = 0; l < p.nl && ok; ++l) {
+          if (s < n && l == p.use[x]) {
+            mma_commit(&bars->v_empty[p.st[l]]);
+          } else {
+            if (!(ok = mbar_wait(&bars->v_full[p.st[l]], p.ph[l], ctl))) break;
+            mbar_arrive(&bars->v_empty[p.st[l]]);
           }
         }
-        pst[0] = st[0]; pst[1] = st[1];
-        pph[0] = ph[0]; pph[1] = ph[1];
-        pshared = shared;
       }
-      // All MMAs must have retired before tensor memory is released.
-      mma_commit(&bars->mma_done);
-      mbar_wait(&bars->mma_done, 0, ctl);
+      mma_commit(&bars->done[1 + x]);
+      mbar_wait(&bars->done[1 + x], 0, ctl);
     }
   } else {
     // ===================== softmax warps =====================
@@ -273,6 +303,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars->s_free[x]);             // S_x(s+1) may now overwrite the S columns
 
       // mask (only boundary tiles) and row max of the raw scores
       const int jl = jmax - kv * kTile;
@@ -281,7 +313,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int c = 0; c < 128; ++c)
           if (c > jl) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
-      // row max as 8 independent chains (latency), then a short tree
       float m8[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) m8[t] = __uint_as_float(sr[0][t]);
@@ -298,6 +329,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       l_true *= alpha;
       l_rnd *= alpha;
       const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+      const float nmref = -mref;
 
       uint32_t keep[4] = {~0u, ~0u, ~0u, ~0u};
       if (a.drop.enabled) {
@@ -307,50 +339,37 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           keep[g >> 2] = (g & 3) == 0 ? bits : (keep[g >> 2] | (bits << ((g & 3) * 8)));
         }
       }
-      // P = exp2(S * tau*log2e - m) in two halves of 64 keys (32 packed words).
+      // P = exp2(S * tau*log2e - m) into registers (64 packed words).
       // l_true sums the unrounded P (for the logsumexp); l_rnd sums exactly the
       // 16-bit values the PV MMA consumes before dropout zeroes some of them
       // (P, or P/(1-p) with dropout), so O / l_rnd is a consistently rounded
       // convex combination of V rows.
       const float pscale = a.drop.enabled ? a.drop.rp : 1.f;
       float lt[4] = {0.f, 0.f, 0.f, 0.f}, lr[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[64];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c2 = 0; c2 < 64; c2 += 2) {
-          const int c = hf * 64 + c2;
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -mref));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2, -mref));
-          lt[(c >> 1) & 1] += p0;
-          lt[2 + ((c >> 1) & 1)] += p1;
-          uint32_t u = a.drop.enabled ? Cvt<T>::pack(p0 * pscale, p1 * pscale) : Cvt<T>::pack(p0, p1);
-          lr[(c >> 1) & 1] += Cvt<T>::lo(u);
-          lr[2 + ((c >> 1) & 1)] += Cvt<T>::hi(u);
-          if (a.drop.enabled) {
-            const uint32_t kb = keep[c >> 5] >> (c & 31);
-            u &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
-          }
-          pk[c2 >> 1] = u;
+      for (int c = 0; c < 128; c += 2) {
+        float x0, x1;
+        fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2, sl2,
+             nmref, nmref);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        lt[(c >> 1) & 1] += p0;
+        lt[2 + ((c >> 1) & 1)] += p1;
+        uint32_t u = a.drop.enabled ? Cvt<T>::pack(p0 * pscale, p1 * pscale) : Cvt<T>::pack(p0, p1);
+        lr[(c >> 1) & 1] += Cvt<T>::lo(u);
+        lr[2 + ((c >> 1) & 1)] += Cvt<T>::hi(u);
+        if (a.drop.enabled) {
+          const uint32_t kb = keep[c >> 5] >> (c & 31);
+          u &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
         }
-        if constexpr (kPTmem) {
-          tmem_st32(tP + hf * 32, pk);
-        } else {
-          uint8_t* pb = smem + C::kP + x * 32768 + hf * 16384;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t off = r * 128 + (((j ^ r) & 7) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                         :: "r"(smem_u32(pb + off)), "r"(pk[j * 4]), "r"(pk[j * 4 + 1]), "r"(pk[j * 4 + 2]),
-                            "r"(pk[j * 4 + 3]) : "memory");
-          }
-        }
+        pk[c >> 1] = u;
       }
-      const float lt0 = lt[0] + lt[1], lt1 = lt[2] + lt[3];
-      const float lr0 = (lr[0] + lr[1]) / pscale, lr1 = (lr[2] + lr[3]) / pscale;
-      l_true += lt0 + lt1;
-      l_rnd += lr0 + lr1;
+      l_true += (lt[0] + lt[1]) + (lt[2] + lt[3]);
+      l_rnd += ((lr[0] + lr[1]) + (lr[2] + lr[3])) / pscale;
 
+      // PV(s-1) must be done before O is rescaled and the P columns reused
+      if (s > 0 && !(ok = warp_wait(&bars->pv_done[x], (uint32_t)(s - 1) & 1u, ctl))) break;
+      tc_fence_after();
       if (rescale) {
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -362,18 +381,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           tmem_st32(tO + hf * 32, o);
         }
       }
-      if (kPTmem || rescale) tmem_wait_st();
-      if constexpr (!kPTmem) fence_proxy_async_smem();
+      tmem_st32(tP, &pk[0]);
+      tmem_st32(tP + 32, &pk[32]);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[x]);
     }
 
     // ---- epilogue: O / l -> 16 bit -> shared -> TMA store; logsumexp
-    named_bar_sync(1 + x, 128);
-    if (!bars->abort) {
+    if (!named_bar_or(1 + x, 128, !ok || bars->abort)) {
       float o[64];
       if (S.n > 0) {
-        if (warp_wait(&bars->o_full[x], 0, ctl)) {
+        if (warp_wait(&bars->pv_done[x], (uint32_t)(S.n - 1) & 1u, ctl)) {
           tc_fence_after();
           uint32_t raw[2][32];
           tmem_ld32(tO, raw[0]);
@@ -427,26 +446,24 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
 }
 
-template <typename T, bool kPTmem>
+template <typename T>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
                      const FwdArgs& a, cudaStream_t s) {
-  using C = FwdCfg<kPTmem>;
-  auto kern = fwd_tc_kernel<T, kPTmem>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDyn);
+  auto kern = fwd_tc_kernel<T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg::kDyn);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(a.npairs * a.B * a.H);
   if (grid == 0) return cudaSuccess;
-  kern<<<grid, kThreads, C::kDyn, s>>>(q, k, v, o, a);
+  kern<<<grid, kThreads, FwdCfg::kDyn, s>>>(q, k, v, o, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_tc(int dtype, bool p_in_tmem, const CUtensorMap& q, const CUtensorMap& k,
-                          const CUtensorMap& v, const CUtensorMap& o, const FwdArgs& a, cudaStream_t s) {
-  if (dtype == FA_DT_BF16)
-    return p_in_tmem ? launch_t<__nv_bfloat16, true>(q, k, v, o, a, s) : launch_t<__nv_bfloat16, false>(q, k, v, o, a, s);
-  return p_in_tmem ? launch_t<__half, true>(q, k, v, o, a, s) : launch_t<__half, false>(q, k, v, o, a, s);
+cudaError_t launch_fwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const CUtensorMap& o, const FwdArgs& a, cudaStream_t s) {
+  if (dtype == FA_DT_BF16) return launch_t<__nv_bfloat16>(q, k, v, o, a, s);
+  return launch_t<__half>(q, k, v, o, a, s);
 }
 
 }  // namespace fa

@@ -88,13 +88,6 @@ def test_non_contiguous_layout(dtype):
     _check_all_heads(_wl(200, dtype, causal=True), layout="bnhd")
 
 
-def test_forward_p_through_shared_memory_variant(monkeypatch):
-    # the alternative build of the forward kernel that stages P in shared memory
-    monkeypatch.setenv("FA_FWD_P_SMEM", "1")
-    _check_all_heads(_wl(300, "bf16", causal=True))
-    _check_all_heads(_wl(257, "f16", dropout_p=0.3))
-
-
 def test_dropout_mask_bit_exact():
     B, H, N = 3, 5, 1000
     for (b, h, row0, nrows, p, seed, off) in [(0, 0, 0, 64, 0.1, 0x5EED, 0), (2, 4, 900, 100, 0.5, 2**63 + 5, 2**40),
