@@ -79,7 +79,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 constexpr uint32_t kColST = 0, kColDP = 128, kColDK = 256, kColDV = 320, kColDQ = 384, kColPT = 448;
 
-template <typename T>
+template <typename T, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -328,7 +328,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       tmem_ld32(tl + kColST + c0, sv[0]);
       tmem_ld32(tl + kColST + c0 + 32, sv[1]);
       uint32_t keep[2] = {~0u, ~0u};
-      if (a.drop.enabled) {
+      if constexpr (kDrop) {
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t kb = 0;
@@ -363,7 +363,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           const uint32_t w0 = Cvt<T>::pack(p[0], p[1]), w1 = Cvt<T>::pack(p[2], p[3]);
           pp[hf * 16 + q4 * 2] = w0;
           pp[hf * 16 + q4 * 2 + 1] = w1;
-          if (a.drop.enabled) {
+          if constexpr (kDrop) {
             const uint32_t kb = keep[hf] >> (q4 * 4);
             const float rp = a.drop.rp;
             pt[q4 * 2] = Cvt<T>::pack((kb & 1u) ? p[0] * rp : 0.f, (kb & 2u) ? p[1] * rp : 0.f);
@@ -397,7 +397,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           const float4 d4 = lds128(s_d + (hf * 32 + q4 * 4) * 4);
           float g[4] = {__uint_as_float(dv[hf][q4 * 4]), __uint_as_float(dv[hf][q4 * 4 + 1]),
                         __uint_as_float(dv[hf][q4 * 4 + 2]), __uint_as_float(dv[hf][q4 * 4 + 3])};
-          if (a.drop.enabled) {
+          if constexpr (kDrop) {
             const uint32_t kb = keep[hf] >> (q4 * 4);
             const float rp = a.drop.rp;
 #pragma unroll
@@ -484,11 +484,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
 }
 
-template <typename T>
+template <typename T, bool kDrop>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
                      const CUtensorMap& dk, const CUtensorMap& dv, const CUtensorMap& dqacc, const BwdArgs& a,
                      cudaStream_t s) {
-  auto kern = bwd_tc_kernel<T>;
+  auto kern = bwd_tc_kernel<T, kDrop>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem::kDyn);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(a.nq * a.B * a.H);
@@ -502,8 +502,12 @@ cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
 cudaError_t launch_bwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
                           const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s) {
-  if (dtype == FA_DT_BF16) return launch_t<__nv_bfloat16>(q, k, v, dout, dk, dv, dqacc, a, s);
-  return launch_t<__half>(q, k, v, dout, dk, dv, dqacc, a, s);
+  const bool d = a.drop.enabled != 0;
+  if (dtype == FA_DT_BF16)
+    return d ? launch_t<__nv_bfloat16, true>(q, k, v, dout, dk, dv, dqacc, a, s)
+             : launch_t<__nv_bfloat16, false>(q, k, v, dout, dk, dv, dqacc, a, s);
+  return d ? launch_t<__half, true>(q, k, v, dout, dk, dv, dqacc, a, s)
+           : launch_t<__half, false>(q, k, v, dout, dk, dv, dqacc, a, s);
 }
 
 }  // namespace fa

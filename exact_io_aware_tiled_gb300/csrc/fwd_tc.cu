@@ -21,9 +21,9 @@
 //       warp 10 / 11 issue O_x += P_x V for slot 0 / 1 (P_x from tensor
 //               memory);
 //   * warps 0-3 / 4-7 run the softmax of slot 0 / 1, one thread per query
-//     row (= tensor-memory lane).  P is computed into registers while the
-//     previous PV MMA still runs; only the O rescale and the P store wait
-//     for it;
+//     row (= tensor-memory lane).  The next S is computed while the
+//     softmax of this one runs; the P store and the O rescale wait for the
+//     previous PV MMA, which normally finished during the row max;
 //   * O is rescaled only when the running row max grows by more than 2^8
 //     (the final O / l and the logsumexp use the same reference max, so the
 //     result is unchanged); O is normalised by the sum of the rounded P that
@@ -123,7 +123,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-template <typename T>
+template <typename T, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -177,8 +177,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   constexpr int ab = Cvt<T>::kAB;
+  // Register split of the 384 x 168 launch budget: the softmax warpgroups
+  // hold a whole 128-column score row per thread; the four TMA / MMA warps
+  // need few registers.  8 x 32 x 224 + 4 x 32 x 56 = 64512 = 384 x 168.
 
-  if (warp == 8) {
+  if (warp >= 8) {
+   regs_dec<56>();
+   if (warp == 8) {
     // ===================== TMA producer =====================
     if (lane == 0) {
       prefetch_tmap(&tmQ);
@@ -279,12 +284,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mma_commit(&bars->done[1 + x]);
       mbar_wait(&bars->done[1 + x], 0, ctl);
     }
+   }
   } else {
+    regs_inc<224>();
     // ===================== softmax warps =====================
     const int x = warp >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;          // row within the tile = TMEM lane
-    const Slot& S = sl[x];
+    const Slot S = x ? sl[1] : sl[0];
     const int i = S.qt * kTile + r;             // global query row
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tS = tmem + x * 256 + lane_off, tP = tS + 128, tO = tS + 192;
@@ -313,12 +320,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int c = 0; c < 128; ++c)
           if (c > jl) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
+      // row max: 8 independent chains of 3-input max, then a short tree
       float m8[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) m8[t] = __uint_as_float(sr[0][t]);
 #pragma unroll
-      for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      for (int c = 8; c < 128; c += 16) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int c0 = c + t, c1 = c + 8 + t;
+          m8[t] = (c1 < 128) ? max3f(m8[t], __uint_as_float(sr[c0 >> 5][c0 & 31]), __uint_as_float(sr[c1 >> 5][c1 & 31]))
+                             : fmaxf(m8[t], __uint_as_float(sr[c0 >> 5][c0 & 31]));
+        }
+      }
+      float mx = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       mx *= sl2;
       // running reference max: moved only when the tile max exceeds it by 2^8
       float m_new = m_run;
@@ -332,44 +347,49 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const float nmref = -mref;
 
       uint32_t keep[4] = {~0u, ~0u, ~0u, ~0u};
-      if (a.drop.enabled) {
+      if constexpr (kDrop) {
 #pragma unroll
         for (int g = 0; g < 16; ++g) {
           const uint32_t bits = dropout_keep8((uint32_t)(kv * 16 + g), row_g, a.drop);
           keep[g >> 2] = (g & 3) == 0 ? bits : (keep[g >> 2] | (bits << ((g & 3) * 8)));
         }
       }
-      // P = exp2(S * tau*log2e - m) into registers (64 packed words).
+      // PV(s-1) must be done before O is rescaled and the P columns reused
+      // (it normally is: it was issued while this step's S was being computed)
+      if (s > 0 && !(ok = warp_wait(&bars->pv_done[x], (uint32_t)(s - 1) & 1u, ctl))) break;
+      tc_fence_after();
+      // P = exp2(S * tau*log2e - m) in two halves of 64 keys (32 packed words).
       // l_true sums the unrounded P (for the logsumexp); l_rnd sums exactly the
       // 16-bit values the PV MMA consumes before dropout zeroes some of them
       // (P, or P/(1-p) with dropout), so O / l_rnd is a consistently rounded
       // convex combination of V rows.
-      const float pscale = a.drop.enabled ? a.drop.rp : 1.f;
+      const float pscale = kDrop ? a.drop.rp : 1.f;
+      // pair accumulators (packed f32x2 adds): two chains each for l_true, l_rnd
       float lt[4] = {0.f, 0.f, 0.f, 0.f}, lr[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[64];
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        float x0, x1;
-        fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2, sl2,
-             nmref, nmref);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        lt[(c >> 1) & 1] += p0;
-        lt[2 + ((c >> 1) & 1)] += p1;
-        uint32_t u = a.drop.enabled ? Cvt<T>::pack(p0 * pscale, p1 * pscale) : Cvt<T>::pack(p0, p1);
-        lr[(c >> 1) & 1] += Cvt<T>::lo(u);
-        lr[2 + ((c >> 1) & 1)] += Cvt<T>::hi(u);
-        if (a.drop.enabled) {
-          const uint32_t kb = keep[c >> 5] >> (c & 31);
-          u &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c2 = 0; c2 < 64; c2 += 2) {
+          const int c = hf * 64 + c2;
+          const int ch = (c >> 1) & 1;       // which of the two accumulator chains
+          float x0, x1;
+          fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2,
+               sl2, nmref, nmref);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          add2(lt[2 * ch], lt[2 * ch + 1], p0, p1);
+          uint32_t u = kDrop ? Cvt<T>::pack(p0 * pscale, p1 * pscale) : Cvt<T>::pack(p0, p1);
+          add2(lr[2 * ch], lr[2 * ch + 1], Cvt<T>::lo(u), Cvt<T>::hi(u));
+          if constexpr (kDrop) {
+            const uint32_t kb = keep[c >> 5] >> (c & 31);
+            u &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
+          }
+          pk[c2 >> 1] = u;
         }
-        pk[c >> 1] = u;
+        tmem_st32(tP + hf * 32, pk);
       }
       l_true += (lt[0] + lt[1]) + (lt[2] + lt[3]);
       l_rnd += ((lr[0] + lr[1]) + (lr[2] + lr[3])) / pscale;
-
-      // PV(s-1) must be done before O is rescaled and the P columns reused
-      if (s > 0 && !(ok = warp_wait(&bars->pv_done[x], (uint32_t)(s - 1) & 1u, ctl))) break;
-      tc_fence_after();
       if (rescale) {
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -381,8 +401,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           tmem_st32(tO + hf * 32, o);
         }
       }
-      tmem_st32(tP, &pk[0]);
-      tmem_st32(tP + 32, &pk[32]);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[x]);
@@ -446,10 +464,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
 }
 
-template <typename T>
+template <typename T, bool kDrop>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
                      const FwdArgs& a, cudaStream_t s) {
-  auto kern = fwd_tc_kernel<T>;
+  auto kern = fwd_tc_kernel<T, kDrop>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg::kDyn);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(a.npairs * a.B * a.H);
@@ -462,8 +480,10 @@ cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
 
 cudaError_t launch_fwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& o, const FwdArgs& a, cudaStream_t s) {
-  if (dtype == FA_DT_BF16) return launch_t<__nv_bfloat16>(q, k, v, o, a, s);
-  return launch_t<__half>(q, k, v, o, a, s);
+  const bool d = a.drop.enabled != 0;
+  if (dtype == FA_DT_BF16)
+    return d ? launch_t<__nv_bfloat16, true>(q, k, v, o, a, s) : launch_t<__nv_bfloat16, false>(q, k, v, o, a, s);
+  return d ? launch_t<__half, true>(q, k, v, o, a, s) : launch_t<__half, false>(q, k, v, o, a, s);
 }
 
 }  // namespace fa
