@@ -14,32 +14,35 @@
 // GB300 mapping (ours): one CTA per (b, h, 128-key tile), looping over the
 // query tiles that see it; the CTAs of one head are adjacent in launch order
 // so its Q / dO tiles and dQ accumulator rows stay in L2.
-//   * warp 8: TMA loads of K, V once and of Q_i, dO_i (+ LSE_i, D_i rows) into
-//     a two-stage ring;
-//   * warp 9: one thread issues the tcgen05 MMAs in the order
-//       dV(i) | S(i+1) | dK(i) | dP(i+1) | dQ(i)
-//     so the next step's S^T and dP^T are computed while the softmax warps
-//     still work on step i;
-//   * warps 0-3 / 4-7: two warpgroups, each owning 64 of the 128 query
-//     columns of every key row (= tensor-memory lane):
+//   * warp 16: TMA loads of K, V once and of Q_i, dO_i (+ LSE_i, D_i rows)
+//     into a two-stage ring;
+//   * three MMA-issuing warps (one thread each; a single issuing thread
+//     cannot keep the tensor pipe busy with N = 64 products):
+//       warp 17: S^T(i+1) = K Q_{i+1}^T and dP^T(i+1) = V dO_{i+1}^T, each
+//                as soon as the softmax warps have read the previous one;
+//       warp 18: dV += P~^T dO_i (A from tensor memory) and
+//                dK += dS^T Q_i (A from the shared dS^T tile);
+//       warp 19: dQ_i = dS K (A = the same tile read MN-major), then the two
+//                TMA reduce-adds of the staged dQ_{i-1} into the float32
+//                accumulator;
+//   * warps 0-15: four warpgroups, each owning 32 of the 128 query columns
+//     of every key row (= tensor-memory lane):
 //       part 1: P from S^T, P~^T (16 bit) into tensor memory for dV;
-//       part 2: dS from dP^T, dS^T (16 bit) into tensor memory for dK (each
-//               warpgroup overwrites only the dP^T columns it read itself)
-//               and into a swizzled shared tile for dQ;
-//       drain:  dQ_i from tensor memory -> x tau -> double-buffered shared
-//               staging;
-//   * warp 10: one thread turns each filled staging buffer into two TMA
-//     reduce-adds into the float32 dQ accumulator.
+//       part 2: dS from dP^T, dS^T (16 bit) into a swizzled shared tile
+//               that both dK and dQ read;
+//       drain:  16 of the 64 columns of dQ_i from tensor memory -> x tau ->
+//               double-buffered shared staging.
 // Tensor memory (512 columns):
-//   S^T 0-127 | dP^T 128-255 (dS^T, 16 bit: queries 0-63 at 128-159,
-//   64-127 at 192-223) | dK 256-319 | dV 320-383 | dQ 384-447 |
-//   P~^T (16 bit) 448-511.
+//   S^T 0-127 | dP^T 128-255 | dK 256-319 | dV 320-383 | dQ 384-447 |
+//   P~^T (16 bit, queries 32w..32w+31 packed at 448+16w .. +16) 448-511.
+// Registers: 96 a thread (640 threads, one CTA per SM).
 #include "common.cuh"
 
 namespace fa {
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 640;
+constexpr int kCompute = 512;   // threads of warps 0-15
 constexpr int NSB = 2;   // Q / dO stages
 
 struct BwdSmem {
@@ -58,8 +61,9 @@ struct BwdSmem {
 struct BBars {
   uint64_t kv_full;
   uint64_t q_full[NSB], q_empty[NSB];
-  uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free, dkv_full, mma_done;
+  uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free, dkv_full, pt_free;
   uint64_t dsm_free;
+  uint64_t done[3];
   uint64_t stg_full[2], stg_free[2];
   uint32_t tmem_base;
   int abort;
@@ -125,22 +129,23 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(&bars->q_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->p_full, kCompute);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->ds_full, 256);
+    mbar_init(&bars->ds_full, kCompute);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 256);
+    mbar_init(&bars->dq_free, kCompute);
     mbar_init(&bars->dkv_full, 1);
-    mbar_init(&bars->mma_done, 1);
-    mbar_init(&bars->dsm_free, 1);
+    mbar_init(&bars->pt_free, 1);
+    mbar_init(&bars->dsm_free, 2);     // dK and dQ both read the shared dS^T tile
+    for (int i = 0; i < 3; ++i) mbar_init(&bars->done[i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->stg_full[i], 256);
+      mbar_init(&bars->stg_full[i], kCompute);
       mbar_init(&bars->stg_free[i], 1);
     }
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 17) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
@@ -150,129 +155,143 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const uint32_t tmem = bars->tmem_base;
   const size_t ld_row0 = (size_t)bh * a.npad;
 
-  if (warp == 8) {
-    // ===================== TMA producer =====================
-    if (lane == 0 && n > 0) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmDO);
-      mbar_expect_tx(&bars->kv_full, 32768);
-      tma_load_4d(smem + L::kK, &tmK, &bars->kv_full, 0, jt * kTile, h, b);
-      tma_load_4d(smem + L::kV, &tmV, &bars->kv_full, 0, jt * kTile, h, b);
-      int issued = 0;
-      for (int t = 0; t < n; ++t) {
-        const int st = t % NSB;
-        const uint32_t ph = (uint32_t)(t / NSB) & 1u;
-        if (!mbar_wait(&bars->q_empty[st], ph ^ 1u, ctl)) break;
-        const int qi = ql.qt(t);
-        mbar_expect_tx(&bars->q_full[st], 32768 + 1024);
-        tma_load_4d(smem + L::kQ + st * 16384, &tmQ, &bars->q_full[st], 0, qi * kTile, h, b);
-        tma_load_4d(smem + L::kDO + st * 16384, &tmDO, &bars->q_full[st], 0, qi * kTile, h, b);
-        bulk_load(smem + L::kLD + st * 1024, a.lse2 + ld_row0 + (size_t)qi * kTile, 512, &bars->q_full[st]);
-        bulk_load(smem + L::kLD + st * 1024 + 512, a.dvec + ld_row0 + (size_t)qi * kTile, 512, &bars->q_full[st]);
-        ++issued;
-      }
-      for (int t = max(0, issued - NSB); t < issued; ++t)
-        mbar_wait(&bars->q_full[t % NSB], (uint32_t)(t / NSB) & 1u, ctl);
-      mbar_wait(&bars->kv_full, 0, ctl);
-    }
-  } else if (warp == 9) {
-    // ===================== MMA issuer =====================
-    if (lane == 0 && n > 0) {
-      constexpr int ab = Cvt<T>::kAB;
-      constexpr uint32_t idST = idesc_f16(128, 128, ab, 0, 0);   // S^T, dP^T (both operands K-major)
-      constexpr uint32_t idKV = idesc_f16(128, 64, ab, 0, 1);    // dV, dK (A from tensor memory, B MN-major)
-      constexpr uint32_t idQ = idesc_f16(128, 64, ab, 1, 1);     // dQ (A MN-major, B MN-major)
-      const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
-      const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
-      const uint32_t sDS = smem_u32(smem + L::kDS);
-      auto issue_st = [&](int st1) {   // S^T = K Q^T
-        const uint32_t q1 = sQ + st1 * 16384;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tmem + kColST, sdesc_sw128(sK + k * 32, 16, 1024), sdesc_sw128(q1 + k * 32, 16, 1024), idST,
-                 k > 0 ? 1u : 0u);
-      };
-      auto issue_dp = [&](int st1) {   // dP^T = V dO^T
-        const uint32_t d1 = sDO + st1 * 16384;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tmem + kColDP, sdesc_sw128(sV + k * 32, 16, 1024), sdesc_sw128(d1 + k * 32, 16, 1024), idST,
-                 k > 0 ? 1u : 0u);
-      };
-      bool ok = mbar_wait(&bars->kv_full, 0, ctl) && mbar_wait(&bars->q_full[0], 0, ctl);
-      if (ok) {
-        tc_fence_after();
-        issue_st(0);
-        mma_commit(&bars->s_full);
-        issue_dp(0);
-        mma_commit(&bars->dp_full);
-      }
-      for (int t = 0; t < n && ok; ++t) {
-        const int st = t % NSB;
-        const uint32_t qb = sQ + st * 16384, db = sDO + st * 16384;
-        const bool more = t + 1 < n;
-        const int st1 = (t + 1) % NSB;
-        // dV += P~^T dO_t  (A = P~^T in tensor memory; K-dim = 128 queries, 8 steps of 16)
-        if (!(ok = mbar_wait(&bars->p_full, (uint32_t)t & 1u, ctl))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + kColDV, tmem + kColPT + k * 8, sdesc_sw128(db + k * 2048, 16384, 1024), idKV,
-                 (t > 0 || k > 0) ? 1u : 0u);
-        // S^T(t+1): its columns were consumed by part 1 of step t
-        if (more) {
-          if (!(ok = mbar_wait(&bars->q_full[st1], (uint32_t)((t + 1) / NSB) & 1u, ctl))) break;
-          tc_fence_after();
-          issue_st(st1);
-          mma_commit(&bars->s_full);
+  if (warp >= 16) {
+    constexpr int ab = Cvt<T>::kAB;
+    constexpr uint32_t idST = idesc_f16(128, 128, ab, 0, 0);   // S^T, dP^T (both operands K-major)
+    constexpr uint32_t idKV = idesc_f16(128, 64, ab, 0, 1);    // dV, dK (A K-major or in tensor memory, B MN-major)
+    constexpr uint32_t idQ = idesc_f16(128, 64, ab, 1, 1);     // dQ (A MN-major, B MN-major)
+    const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+    const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
+    const uint32_t sDS = smem_u32(smem + L::kDS);
+    if (warp == 16) {
+      // ===================== TMA producer =====================
+      if (lane == 0 && n > 0) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmDO);
+        mbar_expect_tx(&bars->kv_full, 32768);
+        tma_load_4d(smem + L::kK, &tmK, &bars->kv_full, 0, jt * kTile, h, b);
+        tma_load_4d(smem + L::kV, &tmV, &bars->kv_full, 0, jt * kTile, h, b);
+        int issued = 0;
+        for (int t = 0; t < n; ++t) {
+          const int st = t % NSB;
+          const uint32_t ph = (uint32_t)(t / NSB) & 1u;
+          if (!mbar_wait(&bars->q_empty[st], ph ^ 1u, ctl)) break;
+          const int qi = ql.qt(t);
+          mbar_expect_tx(&bars->q_full[st], 32768 + 1024);
+          tma_load_4d(smem + L::kQ + st * 16384, &tmQ, &bars->q_full[st], 0, qi * kTile, h, b);
+          tma_load_4d(smem + L::kDO + st * 16384, &tmDO, &bars->q_full[st], 0, qi * kTile, h, b);
+          bulk_load(smem + L::kLD + st * 1024, a.lse2 + ld_row0 + (size_t)qi * kTile, 512, &bars->q_full[st]);
+          bulk_load(smem + L::kLD + st * 1024 + 512, a.dvec + ld_row0 + (size_t)qi * kTile, 512, &bars->q_full[st]);
+          ++issued;
         }
-        // dK += dS^T Q_t  (A = dS^T in tensor memory)
-        if (!(ok = mbar_wait(&bars->ds_full, (uint32_t)t & 1u, ctl))) break;
-        tc_fence_after();
+        for (int t = max(0, issued - NSB); t < issued; ++t)
+          mbar_wait(&bars->q_full[t % NSB], (uint32_t)(t / NSB) & 1u, ctl);
+        mbar_wait(&bars->kv_full, 0, ctl);
+      }
+    } else if (warp == 17) {
+      // ===================== S^T / dP^T issuer =====================
+      if (lane == 0 && n > 0) {
+        auto issue_sd = [&](uint32_t col, uint32_t sA, uint32_t sB) {   // col = sA sB^T, K-dim = d
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + kColDK, tmem + kColDP + (k >> 2) * 64 + (k & 3) * 8, sdesc_sw128(qb + k * 2048, 16384, 1024),
-                 idKV, (t > 0 || k > 0) ? 1u : 0u);
-        // dP^T(t+1): overwrites dS^T(t), which dK(t) above has read (MMAs run in issue order)
-        if (more) {
-          issue_dp(st1);
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + col, sdesc_sw128(sA + k * 32, 16, 1024), sdesc_sw128(sB + k * 32, 16, 1024), idST,
+                   k > 0 ? 1u : 0u);
+        };
+        bool ok = mbar_wait(&bars->kv_full, 0, ctl) && mbar_wait(&bars->q_full[0], 0, ctl);
+        if (ok) {
+          tc_fence_after();
+          issue_sd(kColST, sK, sQ);
+          mma_commit(&bars->s_full);
+          issue_sd(kColDP, sV, sDO);
           mma_commit(&bars->dp_full);
         }
-        // dQ_t = dS K  (M = 128 queries from the MN-major view of dS^T, K-dim = 128 keys)
-        if (t > 0 && !(ok = mbar_wait(&bars->dq_free, (uint32_t)(t - 1) & 1u, ctl))) break;
-        tc_fence_after();
+        for (int t = 0; t + 1 < n && ok; ++t) {
+          const int st1 = (t + 1) % NSB;
+          // S^T(t+1) = K Q_{t+1}^T once part 1 of step t has read S^T(t)
+          if (!(ok = mbar_wait(&bars->p_full, (uint32_t)t & 1u, ctl) &&
+                     mbar_wait(&bars->q_full[st1], (uint32_t)((t + 1) / NSB) & 1u, ctl))) break;
+          tc_fence_after();
+          issue_sd(kColST, sK, sQ + st1 * 16384);
+          mma_commit(&bars->s_full);
+          // dP^T(t+1) = V dO_{t+1}^T once part 2 of step t has read dP^T(t)
+          if (!(ok = mbar_wait(&bars->ds_full, (uint32_t)t & 1u, ctl))) break;
+          tc_fence_after();
+          issue_sd(kColDP, sV, sDO + st1 * 16384);
+          mma_commit(&bars->dp_full);
+        }
+        mma_commit(&bars->done[0]);
+        mbar_wait(&bars->done[0], 0, ctl);
+      }
+    } else if (warp == 18) {
+      // ===================== dV / dK issuer =====================
+      if (lane == 0 && n > 0) {
+        bool ok = true;
+        for (int t = 0; t < n && ok; ++t) {
+          const int st = t % NSB;
+          const uint32_t qb = sQ + st * 16384, db = sDO + st * 16384;
+          // dV += P~^T dO_t  (A = P~^T in tensor memory; K-dim = 128 queries, 8 steps of 16)
+          if (!(ok = mbar_wait(&bars->p_full, (uint32_t)t & 1u, ctl) &&
+                     mbar_wait(&bars->q_full[st], (uint32_t)(t / NSB) & 1u, ctl))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + kColDQ, sdesc_sw128(sDS + k * 2048, 16384, 1024), sdesc_sw128(sK + k * 2048, 16384, 1024),
-                 idQ, k > 0 ? 1u : 0u);
-        mma_commit(&bars->dq_full);
-        mma_commit(&bars->dsm_free);
-        mma_commit(&bars->q_empty[st]);
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + kColDV, tmem + kColPT + k * 8, sdesc_sw128(db + k * 2048, 16384, 1024), idKV,
+                   (t > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bars->pt_free);
+          // dK += dS^T Q_t  (A = dS^T from the shared tile, K-major: chunk k / 4, 32 bytes per 16 queries)
+          if (!(ok = mbar_wait(&bars->ds_full, (uint32_t)t & 1u, ctl))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ss(tmem + kColDK, sdesc_sw128(sDS + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                   sdesc_sw128(qb + k * 2048, 16384, 1024), idKV, (t > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bars->dsm_free);
+          mma_commit(&bars->q_empty[st]);
+        }
+        mma_commit(&bars->dkv_full);
+        mma_commit(&bars->done[1]);
+        mbar_wait(&bars->done[1], 0, ctl);
       }
-      mma_commit(&bars->dkv_full);
-      mma_commit(&bars->mma_done);
-      mbar_wait(&bars->mma_done, 0, ctl);
-    }
-  } else if (warp == 10) {
-    // ===================== dQ reduce issuer =====================
-    if (lane == 0 && n > 0) {
-      prefetch_tmap(&tmDQ);
-      for (int t = 0; t < n; ++t) {
-        const int bi = t & 1;
-        if (!mbar_wait(&bars->stg_full[bi], (uint32_t)(t >> 1) & 1u, ctl)) break;
-        const uint8_t* sb = smem + L::kDQ + bi * 32768;
-        const int qi = ql.qt(t);
-        tma_reduce_add_4d(&tmDQ, sb, 0, qi * kTile, h, b);
-        tma_reduce_add_4d(&tmDQ, sb + 16384, 32, qi * kTile, h, b);
-        bulk_commit();
+    } else {
+      // ===================== dQ issuer + dQ reduce =====================
+      if (lane == 0 && n > 0) {
+        prefetch_tmap(&tmDQ);
+        // staging buffer t % 2 -> two TMA reduce-adds into the float32 accumulator
+        auto reduce = [&](int t) -> bool {
+          const int bi = t & 1;
+          if (!mbar_wait(&bars->stg_full[bi], (uint32_t)(t >> 1) & 1u, ctl)) return false;
+          const uint8_t* sb = smem + L::kDQ + bi * 32768;
+          const int qi = ql.qt(t);
+          tma_reduce_add_4d(&tmDQ, sb, 0, qi * kTile, h, b);
+          tma_reduce_add_4d(&tmDQ, sb + 16384, 32, qi * kTile, h, b);
+          bulk_commit();
+          bulk_wait_read0();
+          mbar_arrive(&bars->stg_free[bi]);
+          return true;
+        };
+        bool ok = true;
+        for (int t = 0; t < n && ok; ++t) {
+          // dQ_t = dS K  (M = 128 queries from the MN-major view of dS^T, K-dim = 128 keys)
+          if (!(ok = mbar_wait(&bars->ds_full, (uint32_t)t & 1u, ctl))) break;
+          if (t > 0 && !(ok = mbar_wait(&bars->dq_free, (uint32_t)(t - 1) & 1u, ctl))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ss(tmem + kColDQ, sdesc_sw128(sDS + k * 2048, 16384, 1024), sdesc_sw128(sK + k * 2048, 16384, 1024),
+                   idQ, k > 0 ? 1u : 0u);
+          mma_commit(&bars->dq_full);
+          mma_commit(&bars->dsm_free);
+          if (t > 0) ok = reduce(t - 1);
+        }
+        if (ok) reduce(n - 1);
+        mma_commit(&bars->done[2]);
+        mbar_wait(&bars->done[2], 0, ctl);
         bulk_wait_read0();
-        mbar_arrive(&bars->stg_free[bi]);
       }
-      bulk_wait0();
     }
-  } else if (warp < 8) {
+  } else {
     // ===================== softmax-gradient warpgroups =====================
-    const int wg = warp >> 2;                 // 0: query columns 0-63, 1: 64-127
+    const int wg = warp >> 2;                 // query columns 32 wg .. 32 wg + 31
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;        // key row within the tile = TMEM lane
     const int j = jt * kTile + r;             // global key
@@ -281,28 +300,31 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const bool key_ok = j < Lk;
     const float sl2 = a.scale_log2;
     const uint32_t bh_rows = (uint32_t)bh * (uint32_t)a.N;
-    const int c0 = wg * 64;                   // first query column of this warpgroup
+    const int c0 = wg * 32;                   // first query column of this warpgroup
+    // 16-byte pieces (w & 1) * 4 .. + 4 of a 128-byte swizzled row belong to this warpgroup
+    const int pc_base = (wg & 1) * 4;
     bool ok = true;
 
-    // dQ_t: tensor memory -> x tau -> staging buffer t % 2 (warp 10 reduces it)
+    // dQ_t: 16 of its 64 columns, tensor memory -> x tau -> staging buffer t % 2
+    // (warp 18 reduces it)
     auto drain_dq = [&](int t) -> bool {
       if (!warp_wait(&bars->dq_full, (uint32_t)t & 1u, ctl)) return false;
       tc_fence_after();
-      uint32_t g[32];
-      tmem_ld32(tl + kColDQ + wg * 32, g);
+      uint32_t g[16];
+      tmem_ld16(tl + kColDQ + wg * 16, g);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->dq_free);
       const int bi = t & 1;
       if (t >= 2 && !warp_wait(&bars->stg_free[bi], (uint32_t)((t - 2) >> 1) & 1u, ctl)) return false;
-      uint8_t* sb = smem + L::kDQ + bi * 32768 + wg * 16384 + r * 128;
+      uint8_t* sb = smem + L::kDQ + bi * 32768 + (wg >> 1) * 16384 + r * 128;
 #pragma unroll
-      for (int pc = 0; pc < 8; ++pc) {
-        const uint32_t off = (((pc ^ r) & 7) << 4);
+      for (int pc4 = 0; pc4 < 4; ++pc4) {
+        const uint32_t off = ((((pc_base + pc4) ^ r) & 7) << 4);
         asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
                      :: "r"(smem_u32(sb + off)),
-                        "f"(__uint_as_float(g[pc * 4]) * a.scale), "f"(__uint_as_float(g[pc * 4 + 1]) * a.scale),
-                        "f"(__uint_as_float(g[pc * 4 + 2]) * a.scale), "f"(__uint_as_float(g[pc * 4 + 3]) * a.scale)
+                        "f"(__uint_as_float(g[pc4 * 4]) * a.scale), "f"(__uint_as_float(g[pc4 * 4 + 1]) * a.scale),
+                        "f"(__uint_as_float(g[pc4 * 4 + 2]) * a.scale), "f"(__uint_as_float(g[pc4 * 4 + 3]) * a.scale)
                      : "memory");
       }
       fence_proxy_async_smem();
@@ -313,7 +335,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     for (int t = 0; t < n && ok; ++t) {
       const int st = t % NSB;
       const int qi = ql.qt(t);
-      // LSE*log2e and D of this warpgroup's 64 query columns, in shared memory
+      // LSE*log2e and D of this warpgroup's 32 query columns, in shared memory
       const uint32_t s_lse = smem_u32(smem + L::kLD + st * 1024) + c0 * 4;
       const uint32_t s_d = s_lse + 512;
       // query column c (relative to c0) is hidden from this key under causal iff c0 + c < qlo
@@ -324,47 +346,42 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (!(ok = warp_wait(&bars->s_full, (uint32_t)t & 1u, ctl) &&
                  warp_wait(&bars->q_full[st], (uint32_t)(t / NSB) & 1u, ctl))) break;
       tc_fence_after();
-      uint32_t sv[2][32];
-      tmem_ld32(tl + kColST + c0, sv[0]);
-      tmem_ld32(tl + kColST + c0 + 32, sv[1]);
-      uint32_t keep[2] = {~0u, ~0u};
+      uint32_t sv[32];
+      tmem_ld32(tl + kColST + c0, sv);
+      uint32_t keep = ~0u;
       if constexpr (kDrop) {
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t kb = 0;
+        uint32_t kb = 0;
 #pragma unroll 4
-          for (int c = 0; c < 32; ++c) {
-            const uint32_t q = (uint32_t)(qi * kTile + c0 + hf * 32 + c);
-            const uint32_t bits = dropout_keep8((uint32_t)j >> 3, bh_rows + q, a.drop);
-            kb |= ((bits >> (j & 7)) & 1u) << c;
-          }
-          keep[hf] = kb;
+        for (int c = 0; c < 32; ++c) {
+          const uint32_t q = (uint32_t)(qi * kTile + c0 + c);
+          const uint32_t bits = dropout_keep8((uint32_t)j >> 3, bh_rows + q, a.drop);
+          kb |= ((bits >> (j & 7)) & 1u) << c;
         }
+        keep = kb;
       }
       tmem_wait_ld();
-      uint32_t pp[32];      // undropped P, 16 bit, kept for part 2
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      uint32_t pp[16];      // undropped P, 16 bit, kept for part 2
+      {
         uint32_t pt[16];    // P~ = Z o P / (1 - p), 16 bit, operand of dV
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 l4 = lds128(s_lse + (hf * 32 + q4 * 4) * 4);
+          const float4 l4 = lds128(s_lse + q4 * 16);
           float x[4];
-          fma2(x[0], x[1], __uint_as_float(sv[hf][q4 * 4]), __uint_as_float(sv[hf][q4 * 4 + 1]), sl2, sl2, -l4.x, -l4.y);
-          fma2(x[2], x[3], __uint_as_float(sv[hf][q4 * 4 + 2]), __uint_as_float(sv[hf][q4 * 4 + 3]), sl2, sl2, -l4.z, -l4.w);
+          fma2(x[0], x[1], __uint_as_float(sv[q4 * 4]), __uint_as_float(sv[q4 * 4 + 1]), sl2, sl2, -l4.x, -l4.y);
+          fma2(x[2], x[3], __uint_as_float(sv[q4 * 4 + 2]), __uint_as_float(sv[q4 * 4 + 3]), sl2, sl2, -l4.z, -l4.w);
           float p[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) p[e] = ex2(x[e]);
           if (any_mask) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              if (!key_ok || c0 + hf * 32 + q4 * 4 + e < qlo) p[e] = 0.f;
+              if (!key_ok || c0 + q4 * 4 + e < qlo) p[e] = 0.f;
           }
           const uint32_t w0 = Cvt<T>::pack(p[0], p[1]), w1 = Cvt<T>::pack(p[2], p[3]);
-          pp[hf * 16 + q4 * 2] = w0;
-          pp[hf * 16 + q4 * 2 + 1] = w1;
+          pp[q4 * 2] = w0;
+          pp[q4 * 2 + 1] = w1;
           if constexpr (kDrop) {
-            const uint32_t kb = keep[hf] >> (q4 * 4);
+            const uint32_t kb = keep >> (q4 * 4);
             const float rp = a.drop.rp;
             pt[q4 * 2] = Cvt<T>::pack((kb & 1u) ? p[0] * rp : 0.f, (kb & 2u) ? p[1] * rp : 0.f);
             pt[q4 * 2 + 1] = Cvt<T>::pack((kb & 4u) ? p[2] * rp : 0.f, (kb & 8u) ? p[3] * rp : 0.f);
@@ -373,7 +390,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             pt[q4 * 2 + 1] = w1;
           }
         }
-        tmem_st16(tl + kColPT + wg * 32 + hf * 16, pt);
+        // dV of the previous step must have read P~^T
+        if (t > 0 && !(ok = warp_wait(&bars->pt_free, (uint32_t)(t - 1) & 1u, ctl))) break;
+        tmem_st16(tl + kColPT + wg * 16, pt);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -382,28 +401,26 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       // ---- part 2: dS from dP^T
       if (!(ok = warp_wait(&bars->dp_full, (uint32_t)t & 1u, ctl))) break;
       tc_fence_after();
-      uint32_t dv[2][32];
-      tmem_ld32(tl + kColDP + c0, dv[0]);
-      tmem_ld32(tl + kColDP + c0 + 32, dv[1]);
+      uint32_t dv[32];
+      tmem_ld32(tl + kColDP + c0, dv);
       tmem_wait_ld();
       // dS^T also goes to the shared tile, once dQ of the previous step has read it
       if (t >= 1 && !(ok = warp_wait(&bars->dsm_free, (uint32_t)(t - 1) & 1u, ctl))) break;
-      uint8_t* dsb = smem + L::kDS + wg * 16384 + r * 128;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      uint8_t* dsb = smem + L::kDS + (wg >> 1) * 16384 + r * 128;
+      {
         uint32_t dsw[16];
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 d4 = lds128(s_d + (hf * 32 + q4 * 4) * 4);
-          float g[4] = {__uint_as_float(dv[hf][q4 * 4]), __uint_as_float(dv[hf][q4 * 4 + 1]),
-                        __uint_as_float(dv[hf][q4 * 4 + 2]), __uint_as_float(dv[hf][q4 * 4 + 3])};
+          const float4 d4 = lds128(s_d + q4 * 16);
+          float g[4] = {__uint_as_float(dv[q4 * 4]), __uint_as_float(dv[q4 * 4 + 1]),
+                        __uint_as_float(dv[q4 * 4 + 2]), __uint_as_float(dv[q4 * 4 + 3])};
           if constexpr (kDrop) {
-            const uint32_t kb = keep[hf] >> (q4 * 4);
+            const uint32_t kb = keep >> (q4 * 4);
             const float rp = a.drop.rp;
 #pragma unroll
             for (int e = 0; e < 4; ++e) g[e] = ((kb >> e) & 1u) ? g[e] * rp : 0.f;
           }
-          const uint32_t w0 = pp[hf * 16 + q4 * 2], w1 = pp[hf * 16 + q4 * 2 + 1];
+          const uint32_t w0 = pp[q4 * 2], w1 = pp[q4 * 2 + 1];
           float y[4];
           sub2(y[0], y[1], g[0], g[1], d4.x, d4.y);
           sub2(y[2], y[3], g[2], g[3], d4.z, d4.w);
@@ -412,17 +429,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           dsw[q4 * 2] = Cvt<T>::pack(y[0], y[1]);
           dsw[q4 * 2 + 1] = Cvt<T>::pack(y[2], y[3]);
         }
-        tmem_st16(tl + kColDP + c0 + hf * 16, dsw);   // inside this warpgroup's own dP^T columns
 #pragma unroll
         for (int pc4 = 0; pc4 < 4; ++pc4) {
-          const int pc = hf * 4 + pc4;
-          const uint32_t off = (((pc ^ r) & 7) << 4);
+          const uint32_t off = ((((pc_base + pc4) ^ r) & 7) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                        :: "r"(smem_u32(dsb + off)), "r"(dsw[pc4 * 4]), "r"(dsw[pc4 * 4 + 1]), "r"(dsw[pc4 * 4 + 2]),
                           "r"(dsw[pc4 * 4 + 3]) : "memory");
         }
       }
-      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->ds_full);
@@ -432,26 +446,27 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
     if (ok && n > 0) ok = drain_dq(n - 1);
 
-    // ---- epilogue: dK (x tau), dV -> 16 bit -> shared -> TMA store
-    if (!named_bar_or(1, 256, !ok || bars->abort)) {
-      uint32_t kraw[32], vraw[32];
+    // ---- epilogue: 16 of the 64 columns of dK (x tau) and dV -> 16 bit ->
+    //      shared -> TMA store
+    if (!named_bar_or(1, kCompute, !ok || bars->abort)) {
+      uint32_t kraw[16], vraw[16];
       bool have = false;
       if (n > 0 && warp_wait(&bars->dkv_full, 0, ctl)) {
         tc_fence_after();
-        tmem_ld32(tl + kColDK + wg * 32, kraw);
-        tmem_ld32(tl + kColDV + wg * 32, vraw);
+        tmem_ld16(tl + kColDK + wg * 16, kraw);
+        tmem_ld16(tl + kColDV + wg * 16, vraw);
         tmem_wait_ld();
         have = true;
       }
       uint8_t* kb = smem + L::kDS;          // dS^T buffers are dead after dkv_full
       uint8_t* vb = smem + L::kDS + 16384;
 #pragma unroll
-      for (int pc4 = 0; pc4 < 4; ++pc4) {
-        const int pc = wg * 4 + pc4;        // 16-byte piece = 8 columns
+      for (int pc2 = 0; pc2 < 2; ++pc2) {
+        const int pc = wg * 2 + pc2;        // 16-byte piece = 8 columns
         uint32_t wk[4], wv[4];
 #pragma unroll
         for (int t2 = 0; t2 < 4; ++t2) {
-          const int c = pc4 * 8 + 2 * t2;   // column within this warpgroup's 32
+          const int c = pc2 * 8 + 2 * t2;   // column within this warpgroup's 16
           const float k0 = have ? __uint_as_float(kraw[c]) * a.scale : 0.f;
           const float k1 = have ? __uint_as_float(kraw[c + 1]) * a.scale : 0.f;
           const float v0 = have ? __uint_as_float(vraw[c]) : 0.f;
@@ -466,19 +481,19 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                      :: "r"(smem_u32(vb + off)), "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3]) : "memory");
       }
       fence_proxy_async_smem();
-      named_bar_sync(1, 256);
+      named_bar_sync(1, kCompute);
       if (threadIdx.x == 0) {
         tma_store_4d(&tmDK, kb, 0, jt * kTile, h, b);
         tma_store_4d(&tmDV, vb, 0, jt * kTile, h, b);
         bulk_commit();
-        bulk_wait0();
+        bulk_wait_read0();   // shared memory must outlive the reads; the writes finish with the grid
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 17) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
