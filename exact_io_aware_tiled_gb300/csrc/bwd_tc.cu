@@ -15,7 +15,7 @@
 // query tiles that see it; the CTAs of one head are adjacent in launch order
 // so its Q / dO tiles and dQ accumulator rows stay in L2.
 //   * warp 16: TMA loads of K, V once and of Q_i, dO_i (+ LSE_i, D_i rows)
-//     into a two-stage ring;
+//     into a three-stage ring;
 //   * three MMA-issuing warps (one thread each; a single issuing thread
 //     cannot keep the tensor pipe busy with N = 64 products):
 //       warp 17: S^T(i+1) = K Q_{i+1}^T and dP^T(i+1) = V dO_{i+1}^T, each
@@ -31,7 +31,7 @@
 //       part 2: dS from dP^T, dS^T (16 bit) into a swizzled shared tile
 //               that both dK and dQ read;
 //       drain:  16 of the 64 columns of dQ_i from tensor memory -> x tau ->
-//               double-buffered shared staging.
+//               shared staging.
 // Tensor memory (512 columns):
 //   S^T 0-127 | dP^T 128-255 | dK 256-319 | dV 320-383 | dQ 384-447 |
 //   P~^T (16 bit, queries 32w..32w+31 packed at 448+16w .. +16) 448-511.
@@ -43,7 +43,8 @@ namespace {
 
 constexpr int kThreads = 640;
 constexpr int kCompute = 512;   // threads of warps 0-15
-constexpr int NSB = 2;   // Q / dO stages
+constexpr int NSB = 3;   // Q / dO stages
+constexpr int NSTG = 1;  // float32 dQ staging buffers
 
 struct BwdSmem {
   static constexpr int kK = 0;
@@ -51,8 +52,8 @@ struct BwdSmem {
   static constexpr int kQ = 32768;                  // NSB x 16 KB
   static constexpr int kDO = kQ + NSB * 16384;      // NSB x 16 KB
   static constexpr int kDS = kDO + NSB * 16384;     // 32 KB: dS^T [2 chunks][128 keys][64 q]
-  static constexpr int kDQ = kDS + 32768;           // 2 x 32 KB: float32 dQ staging [buf][half][128][32]
-  static constexpr int kLD = kDQ + 65536;           // NSB x (LSE2[128] + D[128]) floats
+  static constexpr int kDQ = kDS + 32768;           // NSTG x 32 KB: float32 dQ staging [buf][half][128][32]
+  static constexpr int kLD = kDQ + NSTG * 32768;    // NSB x (LSE2[128] + D[128]) floats
   static constexpr int kBar = kLD + NSB * 1024;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kDyn = kBytes + 1024;
@@ -64,10 +65,12 @@ struct BBars {
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free, dkv_full, pt_free;
   uint64_t dsm_free;
   uint64_t done[3];
-  uint64_t stg_full[2], stg_free[2];
+  uint64_t stg_full[NSTG], stg_free[NSTG];
   uint32_t tmem_base;
   int abort;
 };
+
+static_assert(sizeof(BBars) <= 256, "barrier block overflows its shared-memory slot");
 
 struct QList {
   int n;
@@ -138,7 +141,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(&bars->pt_free, 1);
     mbar_init(&bars->dsm_free, 2);     // dK and dQ both read the shared dS^T tile
     for (int i = 0; i < 3; ++i) mbar_init(&bars->done[i], 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NSTG; ++i) {
       mbar_init(&bars->stg_full[i], kCompute);
       mbar_init(&bars->stg_free[i], 1);
     }
@@ -256,10 +259,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       // ===================== dQ issuer + dQ reduce =====================
       if (lane == 0 && n > 0) {
         prefetch_tmap(&tmDQ);
-        // staging buffer t % 2 -> two TMA reduce-adds into the float32 accumulator
+        // staging buffer t % NSTG -> two TMA reduce-adds into the float32 accumulator
         auto reduce = [&](int t) -> bool {
-          const int bi = t & 1;
-          if (!mbar_wait(&bars->stg_full[bi], (uint32_t)(t >> 1) & 1u, ctl)) return false;
+          const int bi = t % NSTG;
+          if (!mbar_wait(&bars->stg_full[bi], (uint32_t)(t / NSTG) & 1u, ctl)) return false;
           const uint8_t* sb = smem + L::kDQ + bi * 32768;
           const int qi = ql.qt(t);
           tma_reduce_add_4d(&tmDQ, sb, 0, qi * kTile, h, b);
@@ -305,7 +308,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int pc_base = (wg & 1) * 4;
     bool ok = true;
 
-    // dQ_t: 16 of its 64 columns, tensor memory -> x tau -> staging buffer t % 2
+    // dQ_t: 16 of its 64 columns, tensor memory -> x tau -> staging buffer t % NSTG
     // (warp 18 reduces it)
     auto drain_dq = [&](int t) -> bool {
       if (!warp_wait(&bars->dq_full, (uint32_t)t & 1u, ctl)) return false;
@@ -315,8 +318,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->dq_free);
-      const int bi = t & 1;
-      if (t >= 2 && !warp_wait(&bars->stg_free[bi], (uint32_t)((t - 2) >> 1) & 1u, ctl)) return false;
+      const int bi = t % NSTG;
+      if (t >= NSTG && !warp_wait(&bars->stg_free[bi], (uint32_t)((t - NSTG) / NSTG) & 1u, ctl)) return false;
       uint8_t* sb = smem + L::kDQ + bi * 32768 + (wg >> 1) * 16384 + r * 128;
 #pragma unroll
       for (int pc4 = 0; pc4 < 4; ++pc4) {
