@@ -345,12 +345,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const int qlo = a.mask.causal ? (j - qi * kTile) : -1;
       const bool any_mask = !key_ok || qlo > c0;
 
-      // ---- part 1: P from S^T
+      // ---- part 1: P from S^T, in two halves of 16 query columns; the
+      //      tensor-memory load of the second half overlaps the first's math
       if (!(ok = warp_wait(&bars->s_full, (uint32_t)t & 1u, ctl) &&
                  warp_wait(&bars->q_full[st], (uint32_t)(t / NSB) & 1u, ctl))) break;
       tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld32(tl + kColST + c0, sv);
+      uint32_t sv[2][16];
+      tmem_ld16(tl + kColST + c0, sv[0]);
       uint32_t keep = ~0u;
       if constexpr (kDrop) {
         uint32_t kb = 0;
@@ -362,68 +363,77 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         keep = kb;
       }
-      tmem_wait_ld();
       uint32_t pp[16];      // undropped P, 16 bit, kept for part 2
-      {
-        uint32_t pt[16];    // P~ = Z o P / (1 - p), 16 bit, operand of dV
+      uint32_t pt[16];      // P~ = Z o P / (1 - p), 16 bit, operand of dV
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 l4 = lds128(s_lse + q4 * 16);
+      for (int hf = 0; hf < 2; ++hf) {
+        tmem_wait_ld();
+        reg_fence16(sv[hf]);
+        if (hf == 0) tmem_ld16(tl + kColST + c0 + 16, sv[1]);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int cc = hf * 16 + q4 * 4;    // column within this warpgroup's 32
+          const float4 l4 = lds128(s_lse + cc * 4);
           float x[4];
-          fma2(x[0], x[1], __uint_as_float(sv[q4 * 4]), __uint_as_float(sv[q4 * 4 + 1]), sl2, sl2, -l4.x, -l4.y);
-          fma2(x[2], x[3], __uint_as_float(sv[q4 * 4 + 2]), __uint_as_float(sv[q4 * 4 + 3]), sl2, sl2, -l4.z, -l4.w);
+          fma2(x[0], x[1], __uint_as_float(sv[hf][q4 * 4]), __uint_as_float(sv[hf][q4 * 4 + 1]), sl2, sl2, -l4.x, -l4.y);
+          fma2(x[2], x[3], __uint_as_float(sv[hf][q4 * 4 + 2]), __uint_as_float(sv[hf][q4 * 4 + 3]), sl2, sl2, -l4.z, -l4.w);
           float p[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) p[e] = ex2(x[e]);
           if (any_mask) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              if (!key_ok || c0 + q4 * 4 + e < qlo) p[e] = 0.f;
+              if (!key_ok || c0 + cc + e < qlo) p[e] = 0.f;
           }
           const uint32_t w0 = Cvt<T>::pack(p[0], p[1]), w1 = Cvt<T>::pack(p[2], p[3]);
-          pp[q4 * 2] = w0;
-          pp[q4 * 2 + 1] = w1;
+          pp[cc / 2] = w0;
+          pp[cc / 2 + 1] = w1;
           if constexpr (kDrop) {
-            const uint32_t kb = keep >> (q4 * 4);
+            const uint32_t kb = keep >> cc;
             const float rp = a.drop.rp;
-            pt[q4 * 2] = Cvt<T>::pack((kb & 1u) ? p[0] * rp : 0.f, (kb & 2u) ? p[1] * rp : 0.f);
-            pt[q4 * 2 + 1] = Cvt<T>::pack((kb & 4u) ? p[2] * rp : 0.f, (kb & 8u) ? p[3] * rp : 0.f);
+            pt[cc / 2] = Cvt<T>::pack((kb & 1u) ? p[0] * rp : 0.f, (kb & 2u) ? p[1] * rp : 0.f);
+            pt[cc / 2 + 1] = Cvt<T>::pack((kb & 4u) ? p[2] * rp : 0.f, (kb & 8u) ? p[3] * rp : 0.f);
           } else {
-            pt[q4 * 2] = w0;
-            pt[q4 * 2 + 1] = w1;
+            pt[cc / 2] = w0;
+            pt[cc / 2 + 1] = w1;
           }
         }
-        // dV of the previous step must have read P~^T
-        if (t > 0 && !(ok = warp_wait(&bars->pt_free, (uint32_t)(t - 1) & 1u, ctl))) break;
-        tmem_st16(tl + kColPT + wg * 16, pt);
       }
+      // dV of the previous step must have read P~^T
+      if (t > 0 && !(ok = warp_wait(&bars->pt_free, (uint32_t)(t - 1) & 1u, ctl))) break;
+      tmem_st16(tl + kColPT + wg * 16, pt);
+      // dP^T(t) is usually complete by now: start its first load before the store is waited on
+      if (!(ok = warp_wait(&bars->dp_full, (uint32_t)t & 1u, ctl))) break;
+      tc_fence_after();
+      uint32_t dv[2][16];
+      tmem_ld16(tl + kColDP + c0, dv[0]);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full);
 
-      // ---- part 2: dS from dP^T
-      if (!(ok = warp_wait(&bars->dp_full, (uint32_t)t & 1u, ctl))) break;
-      tc_fence_after();
-      uint32_t dv[32];
-      tmem_ld32(tl + kColDP + c0, dv);
-      tmem_wait_ld();
+      // ---- part 2: dS from dP^T, in the same two halves
       // dS^T also goes to the shared tile, once dQ of the previous step has read it
       if (t >= 1 && !(ok = warp_wait(&bars->dsm_free, (uint32_t)(t - 1) & 1u, ctl))) break;
       uint8_t* dsb = smem + L::kDS + (wg >> 1) * 16384 + r * 128;
-      {
-        uint32_t dsw[16];
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 d4 = lds128(s_d + q4 * 16);
-          float g[4] = {__uint_as_float(dv[q4 * 4]), __uint_as_float(dv[q4 * 4 + 1]),
-                        __uint_as_float(dv[q4 * 4 + 2]), __uint_as_float(dv[q4 * 4 + 3])};
+      for (int hf = 0; hf < 2; ++hf) {
+        tmem_wait_ld();
+        reg_fence16(dv[hf]);
+        if (hf == 0) tmem_ld16(tl + kColDP + c0 + 16, dv[1]);
+        uint32_t dsw[8];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int cc = hf * 16 + q4 * 4;
+          const float4 d4 = lds128(s_d + cc * 4);
+          float g[4] = {__uint_as_float(dv[hf][q4 * 4]), __uint_as_float(dv[hf][q4 * 4 + 1]),
+                        __uint_as_float(dv[hf][q4 * 4 + 2]), __uint_as_float(dv[hf][q4 * 4 + 3])};
           if constexpr (kDrop) {
-            const uint32_t kb = keep >> (q4 * 4);
+            const uint32_t kb = keep >> cc;
             const float rp = a.drop.rp;
 #pragma unroll
             for (int e = 0; e < 4; ++e) g[e] = ((kb >> e) & 1u) ? g[e] * rp : 0.f;
           }
-          const uint32_t w0 = pp[q4 * 2], w1 = pp[q4 * 2 + 1];
+          const uint32_t w0 = pp[cc / 2], w1 = pp[cc / 2 + 1];
           float y[4];
           sub2(y[0], y[1], g[0], g[1], d4.x, d4.y);
           sub2(y[2], y[3], g[2], g[3], d4.z, d4.w);
@@ -433,11 +443,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           dsw[q4 * 2 + 1] = Cvt<T>::pack(y[2], y[3]);
         }
 #pragma unroll
-        for (int pc4 = 0; pc4 < 4; ++pc4) {
-          const uint32_t off = ((((pc_base + pc4) ^ r) & 7) << 4);
+        for (int pc2 = 0; pc2 < 2; ++pc2) {
+          const uint32_t off = ((((pc_base + hf * 2 + pc2) ^ r) & 7) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                       :: "r"(smem_u32(dsb + off)), "r"(dsw[pc4 * 4]), "r"(dsw[pc4 * 4 + 1]), "r"(dsw[pc4 * 4 + 2]),
-                          "r"(dsw[pc4 * 4 + 3]) : "memory");
+                       :: "r"(smem_u32(dsb + off)), "r"(dsw[pc2 * 4]), "r"(dsw[pc2 * 4 + 1]), "r"(dsw[pc2 * 4 + 2]),
+                          "r"(dsw[pc2 * 4 + 3]) : "memory");
         }
       }
       fence_proxy_async_smem();
