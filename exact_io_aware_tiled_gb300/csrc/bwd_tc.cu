@@ -316,6 +316,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       uint32_t g[16];
       tmem_ld16(tl + kColDQ + wg * 16, g);
       tmem_wait_ld();
+      reg_fence16(g);
       tc_fence_before();
       mbar_arrive(&bars->dq_free);
       const int bi = t % NSTG;
@@ -469,6 +470,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tmem_ld16(tl + kColDK + wg * 16, kraw);
         tmem_ld16(tl + kColDV + wg * 16, vraw);
         tmem_wait_ld();
+        reg_fence16(kraw);
+        reg_fence16(vraw);
         have = true;
       }
       uint8_t* kb = smem + L::kDS;          // dS^T buffers are dead after dkv_full

@@ -310,6 +310,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
       tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) reg_fence32(sr[cc]);
       tc_fence_before();
       mbar_arrive(&bars->s_free[x]);             // S_x(s+1) may now overwrite the S columns
 
@@ -396,6 +398,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           uint32_t o[32];
           tmem_ld32(tO + hf * 32, o);
           tmem_wait_ld();
+          reg_fence32(o);
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
           tmem_st32(tO + hf * 32, o);
@@ -416,6 +419,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           tmem_ld32(tO, raw[0]);
           tmem_ld32(tO + 32, raw[1]);
           tmem_wait_ld();
+          reg_fence32(raw[0]);
+          reg_fence32(raw[1]);
           const float inv = l_rnd > 0.f ? 1.f / l_rnd : 0.f;
 #pragma unroll
           for (int c = 0; c < 64; ++c) o[c] = __uint_as_float(raw[c >> 5][c & 31]) * inv;
