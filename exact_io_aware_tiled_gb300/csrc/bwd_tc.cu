@@ -16,8 +16,10 @@
 // so its Q / dO tiles and dQ accumulator rows stay in L2.
 //   * warp 16: TMA loads of K, V once and of Q_i, dO_i (+ LSE_i, D_i rows)
 //     into a three-stage ring;
-//   * three MMA-issuing warps (one thread each; a single issuing thread
-//     cannot keep the tensor pipe busy with N = 64 products):
+//   * three MMA-issuing warps (one thread each): consecutive MMAs into the
+//     same accumulator complete about 126 cycles apart whatever their N, so
+//     each product is a latency chain, and independent chains are issued
+//     from separate warps so that they overlap:
 //       warp 17: S^T(i+1) = K Q_{i+1}^T and dP^T(i+1) = V dO_{i+1}^T, each
 //                as soon as the softmax warps have read the previous one;
 //       warp 18: dV += P~^T dO_i (A from tensor memory) and

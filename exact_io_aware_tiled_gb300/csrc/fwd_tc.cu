@@ -14,8 +14,10 @@
 //   * warp 8 (one thread) streams K/V tiles with TMA into a ring of NS
 //     stages; a stage is shared by both slots when both need the same KV tile
 //     at the same step;
-//   * tcgen05 MMAs are issued by three warps, because one issuing thread
-//     sustains only about one MMA per ~100 cycles whatever its size:
+//   * tcgen05 MMAs are issued by three warps: consecutive MMAs that
+//     accumulate into the same tensor-memory tile complete about 126 cycles
+//     apart whatever their N (measured on GB300), so each product is a
+//     latency chain and independent chains are issued from separate warps:
 //       warp 9  issues S_x = Q_x K^T for both slots, as soon as the softmax
 //               has copied the previous S_x into registers;
 //       warp 10 / 11 issue O_x += P_x V for slot 0 / 1 (P_x from tensor
