@@ -17,7 +17,8 @@ pages by eye rather than to be fast:
                      and the dropout keep-mask mapping used by the method.
 * ``traffic``     -- instrumented HBM element counts of the naive and tiled
                      algorithms, for the pages' byte-accounting worked numbers.
-* ``masks``       -- the causal / key-padding / block-sparse mask definitions.
+* ``masks``       -- the causal / sliding-window / key-padding / block-sparse
+                     mask definitions.
 
 Parity status of each function is stated in its own docstring ("pinned by ...").
 """

@@ -12,6 +12,12 @@ head in float64, exactly as the "standard attention" the pages describe
 
   1. S = tau * Q K^T, tau = 1/sqrt(d) unless given.
   2. S_ij = -inf where (i, j) is masked (``oracle.masks``).
+  Grouped-query attention (living-dl-book, efficient attention, section 6:
+  the h query heads form h_kv = h / g groups, each sharing one K head and one
+  V head): query head h reads K and V head h // g, and the gradient of a
+  shared K or V head is the sum of its g query heads' contributions
+  (``attention_fwd`` / ``attention_bwd``; the per-head functions take the
+  head's own K and V rows).
   3. m_i = max_j S_ij;  P_ij = exp(S_ij - m_i) / sum_j exp(S_ij - m_i);
      LSE_i = m_i + ln sum_j exp(S_ij - m_i)  (natural log, tau-scaled units).
      A row with no visible key has P_i = 0, O_i = 0, LSE_i = -inf and zero
@@ -65,10 +71,22 @@ class Spec:
     seed: int = 0
     offset: int = 0
     fixed_keep: Optional[np.ndarray] = field(default=None, repr=False)  # [B,H,N,N] test hook
+    H_kv: Optional[int] = None               # K/V heads (grouped-query); None -> H
+    window: int = 0                          # sliding window of keys (0 = none)
 
     @property
     def tau(self) -> float:
         return float(1.0 / np.sqrt(self.d)) if self.scale is None else float(self.scale)
+
+    @property
+    def hkv(self) -> int:
+        return self.H if self.H_kv is None else int(self.H_kv)
+
+    @property
+    def group(self) -> int:
+        """Query heads per K/V head (g); query head h reads K/V head h // g."""
+        assert self.H % self.hkv == 0, "H must be a multiple of H_kv"
+        return self.H // self.hkv
 
 
 def _f64(x):
@@ -78,7 +96,7 @@ def _f64(x):
 def visible(spec: Spec, b, rows, cols):
     L = None if spec.seqlens_k is None else int(spec.seqlens_k[b])
     return _masks.visible(rows, cols, causal=spec.causal, seqlen_k=L,
-                          block_mask=spec.block_mask, block_size=spec.block_size)
+                          block_mask=spec.block_mask, block_size=spec.block_size, window=spec.window)
 
 
 def keep(spec: Spec, b, h, rows, cols):
@@ -192,22 +210,31 @@ def head_backward(spec: Spec, b, h, q, k, v, do, rows=None, cols=None):
 
 
 def attention_fwd(spec: Spec, q, k, v):
-    """O [B,H,N,d] and LSE [B,H,N] for the whole problem."""
+    """O [B,H,N,d] and LSE [B,H,N] for the whole problem (k, v: [B,H_kv,N,d])."""
     O = np.zeros((spec.B, spec.H, spec.N, spec.d))
     L = np.zeros((spec.B, spec.H, spec.N))
+    g = spec.group
     for b in range(spec.B):
         for h in range(spec.H):
-            O[b, h], L[b, h] = head_forward(spec, b, h, q[b, h], k[b, h], v[b, h])
+            O[b, h], L[b, h] = head_forward(spec, b, h, q[b, h], k[b, h // g], v[b, h // g])
     return O, L
 
 
 def attention_bwd(spec: Spec, q, k, v, do):
-    """dQ, dK, dV [B,H,N,d] and D [B,H,N] for the whole problem."""
+    """dQ [B,H,N,d], dK and dV [B,H_kv,N,d] and D [B,H,N] for the whole problem.
+
+    The gradient of a K/V head shared by g query heads sums their contributions.
+    """
     shp = (spec.B, spec.H, spec.N, spec.d)
-    dq, dk, dv = np.zeros(shp), np.zeros(shp), np.zeros(shp)
+    dq = np.zeros(shp)
+    dk = np.zeros((spec.B, spec.hkv, spec.N, spec.d))
+    dv = np.zeros_like(dk)
     D = np.zeros(shp[:3])
+    g = spec.group
     for b in range(spec.B):
         for h in range(spec.H):
-            g = head_backward(spec, b, h, q[b, h], k[b, h], v[b, h], do[b, h])
-            dq[b, h], dk[b, h], dv[b, h], D[b, h] = g["dq"], g["dk"], g["dv"], g["D"]
+            r = head_backward(spec, b, h, q[b, h], k[b, h // g], v[b, h // g], do[b, h])
+            dq[b, h], D[b, h] = r["dq"], r["D"]
+            dk[b, h // g] += r["dk"]
+            dv[b, h // g] += r["dv"]
     return dq, dk, dv, D

@@ -1,4 +1,5 @@
-"""Mask definitions of the method (causal, key padding, block-sparse).
+"""Mask definitions of the method (causal, sliding window, key padding,
+block-sparse).
 
 TEST INFRASTRUCTURE (see ``oracle/__init__.py``).
 
@@ -14,7 +15,12 @@ butterfly pattern, agihunt.info, paragraph on block-sparse):
   query rows i >= L_b are computed normally;
 * block-sparse keeps whole ``bs`` x ``bs`` blocks: (i, j) visible iff
   kept[i // bs, j // bs];
-* the three combine by logical AND.
+* a sliding window of ``w`` keys (lynx-cortex, "Problemas de práctica", the
+  sliding-window exercise: each query tile then reads only the K/V tiles
+  that overlap its window) is read as the local causal window: key j is
+  visible to query i iff i - w < j, combined with the causal j <= i, so a
+  query sees itself and the w - 1 keys before it;
+* the masks combine by logical AND.
 """
 from __future__ import annotations
 
@@ -29,13 +35,15 @@ def butterfly_block_mask(nblocks):
     return (x == 0) | ((x & (x - 1)) == 0)
 
 
-def visible(rows, cols, *, causal=False, seqlen_k=None, block_mask=None, block_size=128):
+def visible(rows, cols, *, causal=False, seqlen_k=None, block_mask=None, block_size=128, window=0):
     """Boolean [len(rows), len(cols)] visibility of (query row, key col)."""
     rows = np.asarray(rows, dtype=np.int64)[:, None]
     cols = np.asarray(cols, dtype=np.int64)[None, :]
     m = np.ones((rows.shape[0], cols.shape[1]), dtype=bool)
     if causal:
         m &= cols <= rows
+    if window:
+        m &= cols > rows - int(window)
     if seqlen_k is not None:
         m &= cols < int(seqlen_k)
     if block_mask is not None:

@@ -30,6 +30,10 @@ MUTATIONS = [
     ("philox.py", "c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0",
      "c0, c1, c2, c3 = hi0 ^ c1 ^ k0, lo1, hi1 ^ c3 ^ k1, lo0"),
     ("philox.py", "return half >= np.uint64(T)", "return half > np.uint64(T)"),
+    ("masks.py", "m &= cols > rows - int(window)", "m &= cols >= rows - int(window)"),
+    ("attention.py", "dk[b, h // g] += r[\"dk\"]", "dk[b, h // g] = r[\"dk\"]"),
+    ("attention.py", "O[b, h], L[b, h] = head_forward(spec, b, h, q[b, h], k[b, h // g], v[b, h // g])",
+     "O[b, h], L[b, h] = head_forward(spec, b, h, q[b, h], k[b, h % spec.hkv], v[b, h % spec.hkv])"),
 ]
 
 
@@ -45,7 +49,8 @@ def test_pins_catch_planted_mistake(tmp_path, fname, old, new):
     assert src.count(old) == 1, "mutation anchor not found: " + old
     p.write_text(src.replace(old, new))
     tests = [str(dst / "tests" / t) for t in ("test_oracle_attention.py", "test_oracle_tiled.py",
-                                             "test_oracle_philox.py", "test_oracle_traffic.py")]
+                                             "test_oracle_philox.py", "test_oracle_traffic.py",
+                                             "test_oracle_gqa_window.py")]
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "-m", "not slow", *tests], cwd=dst, capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, "planted mistake survived every pin:\n" + r.stdout[-2000:]
