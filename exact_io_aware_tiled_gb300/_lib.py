@@ -38,6 +38,9 @@ class fa_params(ctypes.Structure):
         ("block_size", ctypes.c_int32),
         ("o_f32", ctypes.c_void_p),
         ("prof_start", ctypes.c_void_p), ("prof_stop", ctypes.c_void_p),
+        ("H_kv", ctypes.c_int32),
+        ("kv_stride_b", ctypes.c_int64), ("kv_stride_h", ctypes.c_int64), ("kv_stride_n", ctypes.c_int64),
+        ("window", ctypes.c_int32),
     ]
 
 
@@ -95,13 +98,17 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def make_params(q: torch.Tensor, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0,
-                block_mask=None, scale=None, o_f32=None, prof=None) -> fa_params:
+def make_params(q: torch.Tensor, *, k: Optional[torch.Tensor] = None, causal=False, seqlens_k=None, dropout_p=0.0,
+                seed=0, offset=0, block_mask=None, scale=None, o_f32=None, prof=None, window=0) -> fa_params:
     B, H, N, d = q.shape
     p = fa_params()
     p.B, p.H, p.N, p.d = B, H, N, d
     p.dtype = DTYPE_CODE[q.dtype]
     p.stride_b, p.stride_h, p.stride_n = q.stride(0), q.stride(1), q.stride(2)
+    if k is not None:   # K/V (and dK/dV) layout; fewer heads = grouped-query attention
+        p.H_kv = k.shape[1]
+        p.kv_stride_b, p.kv_stride_h, p.kv_stride_n = k.stride(0), k.stride(1), k.stride(2)
+    p.window = int(window)
     p.scale = 0.0 if scale is None else float(scale)
     p.causal = 1 if causal else 0
     p.seqlens_k = None if seqlens_k is None else seqlens_k.data_ptr()
@@ -117,13 +124,27 @@ def make_params(q: torch.Tensor, *, causal=False, seqlens_k=None, dropout_p=0.0,
 
 
 def _same_layout(ts):
-    """All [B,H,N,d] tensors must share one stride set with a contiguous last dim."""
+    """Tensors of one group must share one stride set with a contiguous last dim."""
     ref = ts[0]
     ok = all(t.shape == ref.shape and t.stride() == ref.stride() and t.dtype == ref.dtype for t in ts)
     ok = ok and ref.stride(3) == 1
     if ok:
         return ts
     return [t.contiguous() for t in ts]
+
+
+def _layouts(q_like, kv):
+    """Q-side tensors ([B,H,N,d]) and K/V-side tensors ([B,H_kv,N,d], H % H_kv == 0)."""
+    q_like = _same_layout(q_like)
+    kv = _same_layout(kv)
+    q, k = q_like[0], kv[0]
+    if k.dim() != 4 or (k.shape[0], k.shape[2], k.shape[3]) != (q.shape[0], q.shape[2], q.shape[3]):
+        raise ValueError("k, v must be [B, H_kv, N, d] with the B, N, d of q")
+    if k.shape[1] < 1 or q.shape[1] % k.shape[1] != 0:
+        raise ValueError("the number of query heads must be a multiple of the number of K/V heads")
+    if k.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype")
+    return q_like, kv
 
 
 def _check(q, name="q"):
@@ -150,18 +171,21 @@ def _aux(seqlens_k, block_mask, q):
 
 
 def fwd(q, k, v, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0, block_mask=None,
-        scale=None, return_o_f32=False, stream=None, prof=None):
-    """O, LSE (and optionally the float32 O before rounding) via fa_fwd."""
+        scale=None, return_o_f32=False, stream=None, prof=None, window=0):
+    """O, LSE (and optionally the float32 O before rounding) via fa_fwd.
+
+    k, v may have fewer heads than q (grouped-query attention); ``window`` > 0
+    (with ``causal``) restricts query i to keys i - window < j <= i."""
     _check(q)
-    q, k, v = _same_layout([q, k, v])
+    (q,), (k, v) = _layouts([q], [k, v])
     lib = load()
     seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
     B, H, N, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
     o32 = torch.empty((B, H, N, d), device=q.device, dtype=torch.float32) if return_o_f32 else None
-    p = make_params(q, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
-                    block_mask=block_mask, scale=scale, o_f32=o32, prof=prof)
+    p = make_params(q, k=k, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
+                    block_mask=block_mask, scale=scale, o_f32=o32, prof=prof, window=window)
     wsz = lib.fa_fwd_workspace_size(ctypes.byref(p))
     ws = torch.empty(wsz, device=q.device, dtype=torch.uint8)
     st = lib.fa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), wsz, _stream(stream))
@@ -172,16 +196,16 @@ def fwd(q, k, v, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=
 
 
 def bwd(q, k, v, o, do, lse, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0, block_mask=None,
-        scale=None, stream=None, prof=None):
-    """dQ, dK, dV via fa_bwd."""
+        scale=None, stream=None, prof=None, window=0):
+    """dQ, dK, dV via fa_bwd (dK, dV have the K/V heads of k, v)."""
     _check(q)
-    q, k, v, o, do = _same_layout([q, k, v, o, do])
+    (q, o, do), (k, v) = _layouts([q, o, do], [k, v])
     lib = load()
     seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
     lse = lse.contiguous()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    p = make_params(q, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
-                    block_mask=block_mask, scale=scale, prof=prof)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    p = make_params(q, k=k, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
+                    block_mask=block_mask, scale=scale, prof=prof, window=window)
     wsz = lib.fa_bwd_workspace_size(ctypes.byref(p))
     ws = torch.empty(wsz, device=q.device, dtype=torch.uint8)
     st = lib.fa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
@@ -217,22 +241,22 @@ def default_scale(d: int) -> float:
 
 
 def bwd_noalloc(q, k, v, o, do, lse, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0,
-                block_mask=None, scale=None, stream=None):
+                block_mask=None, scale=None, stream=None, window=0):
     """dQ, dK, dV via fa_bwd_noalloc: the backward pass using the library's own
     fixed device scratch array instead of a caller-allocated workspace (for
     callers that cannot allocate device memory; problems needing more than
     64 MiB of scratch are refused)."""
     _check(q)
-    q, k, v, o, do = _same_layout([q, k, v, o, do])
+    (q, o, do), (k, v) = _layouts([q, o, do], [k, v])
     lib = load()
     fn = lib.fa_bwd_noalloc
     fn.argtypes = [ctypes.POINTER(fa_params)] + [ctypes.c_void_p] * 10
     fn.restype = ctypes.c_int
     seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
     lse = lse.contiguous()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    p = make_params(q, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
-                    block_mask=block_mask, scale=scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    p = make_params(q, k=k, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
+                    block_mask=block_mask, scale=scale, window=window)
     st = fn(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
             _stream(stream))
     if st != FA_OK:

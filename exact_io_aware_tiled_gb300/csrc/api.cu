@@ -72,6 +72,10 @@ bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u
 
 int elem_bytes(int dt) { return dt == FA_DT_F32 ? 4 : 2; }
 
+int hkv_of(const fa_params* p) { return p->H_kv == 0 ? p->H : p->H_kv; }
+
+bool kv_strides_given(const fa_params* p) { return p->kv_stride_b || p->kv_stride_h || p->kv_stride_n; }
+
 // Shape / dtype / stride / alignment checks shared by fa_fwd and fa_bwd.
 fa_status check_params(const fa_params* p) {
   if (p == nullptr) return FA_ERR_INVALID_ARG;
@@ -86,16 +90,34 @@ fa_status check_params(const fa_params* p) {
   const int64_t unit = 16 / elem_bytes(p->dtype);   // elements per 16 bytes
   if (p->stride_n % unit || p->stride_h % unit || p->stride_b % unit) return FA_ERR_MISALIGNED;
   if (p->o_f32 != nullptr && !aligned16(p->o_f32)) return FA_ERR_MISALIGNED;
+  const int hkv = hkv_of(p);
+  if (hkv < 1 || p->H % hkv != 0) return FA_ERR_INVALID_ARG;
+  if (kv_strides_given(p)) {
+    if (p->kv_stride_n < p->d || p->kv_stride_h < 1 || p->kv_stride_b < 1) return FA_ERR_INVALID_ARG;
+    if (p->kv_stride_n % unit || p->kv_stride_h % unit || p->kv_stride_b % unit) return FA_ERR_MISALIGNED;
+  } else if (hkv != p->H) {
+    return FA_ERR_INVALID_ARG;   // K/V with fewer heads need their own strides
+  }
+  if (p->window < 0) return FA_ERR_INVALID_ARG;
+  if (p->window > 0 && !p->causal) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
-Strides strides_of(const fa_params* p) {
-  // Singleton dimensions carry whatever stride the caller had; normalise them
-  // so every stride handed to TMA is a valid, representable byte stride.
-  Strides s{p->stride_b, p->stride_h, p->stride_n};
-  if (p->H == 1) s.h = (int64_t)p->N * s.n;
-  if (p->B == 1) s.b = (int64_t)p->H * s.h;
+// Singleton dimensions carry whatever stride the caller had; normalise them
+// so every stride handed to TMA is a valid, representable byte stride.
+Strides normalised(Strides s, const fa_params* p, int heads) {
+  if (heads == 1) s.h = (int64_t)p->N * s.n;
+  if (p->B == 1) s.b = (int64_t)heads * s.h;
   return s;
+}
+
+// Strides of Q, O, dO, dQ ([B,H,N,d]).
+Strides strides_of(const fa_params* p) { return normalised({p->stride_b, p->stride_h, p->stride_n}, p, p->H); }
+
+// Strides of K, V, dK, dV ([B,H_kv,N,d]).
+Strides kv_strides_of(const fa_params* p) {
+  if (!kv_strides_given(p)) return strides_of(p);
+  return normalised({p->kv_stride_b, p->kv_stride_h, p->kv_stride_n}, p, hkv_of(p));
 }
 
 float scale_of(const fa_params* p) {
@@ -115,12 +137,12 @@ DropoutArgs dropout_of(const fa_params* p) {
   return d;
 }
 
-// 4-D map over a [B,H,N,cols] tensor: dims (cols, N, H, B), box (box_c, 128, 1, 1), 128-byte swizzle.
+// 4-D map over a [B,heads,N,cols] tensor: dims (cols, N, heads, B), box (box_c, 128, 1, 1), 128-byte swizzle.
 fa_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int cols, int box_c,
-                   const fa_params* p, Strides s) {
+                   const fa_params* p, int heads, Strides s) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return FA_ERR_CUDA;
-  cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)p->N, (cuuint64_t)p->H, (cuuint64_t)p->B};
+  cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)p->N, (cuuint64_t)heads, (cuuint64_t)p->B};
   cuuint64_t strides[3] = {(cuuint64_t)(s.n * esize), (cuuint64_t)(s.h * esize), (cuuint64_t)(s.b * esize)};
   cuuint32_t box[4] = {(cuuint32_t)box_c, (cuuint32_t)kTile, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
@@ -130,15 +152,16 @@ fa_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status map16(CUtensorMap* m, const void* base, const fa_params* p, Strides s) {
+fa_status map16(CUtensorMap* m, const void* base, const fa_params* p, int heads, Strides s) {
   const CUtensorMapDataType dt =
       p->dtype == FA_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return make_map(m, base, dt, 2, kHeadDim, kHeadDim, p, s);
+  return make_map(m, base, dt, 2, kHeadDim, kHeadDim, p, heads, s);
 }
 
 MaskArgs mask_of(const fa_params* p, const Layout& L, uint8_t* ws) {
   MaskArgs m{};
   m.causal = p->causal ? 1 : 0;
+  m.window = p->window;
   m.seqlens_k = p->seqlens_k;
   if (L.sparse) {
     m.row_list = reinterpret_cast<const int16_t*>(ws + L.rlist);
@@ -201,10 +224,12 @@ fa_status fa_fwd(const fa_params* p, const void* q, const void* k, const void* v
   if (ws == nullptr || ws_bytes < L.total || !aligned16(ws)) return FA_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  const Strides sd = strides_of(p);
+  const Strides sd = strides_of(p), skv = kv_strides_of(p);
+  const int hkv = hkv_of(p);
 
   FwdArgs a{};
   a.B = p->B; a.H = p->H; a.N = p->N;
+  a.group = p->H / hkv;
   a.nq = L.nq;
   a.npairs = (L.nq + 1) / 2;
   a.scale_log2 = scale_of(p) * 1.4426950408889634f;
@@ -218,11 +243,12 @@ fa_status fa_fwd(const fa_params* p, const void* q, const void* k, const void* v
   if (p->dtype == FA_DT_F32) {
     if (p->o_f32 != nullptr) return FA_ERR_UNSUPPORTED;   // O is already float32
     ProfScope prof(p, st);
-    return cuda_status(launch_fwd_simt((const float*)q, (const float*)k, (const float*)v, (float*)o, sd, a, st));
+    return cuda_status(
+        launch_fwd_simt((const float*)q, (const float*)k, (const float*)v, (float*)o, sd, skv, a, st));
   }
   CUtensorMap mq, mk, mv, mo;
-  if ((s = map16(&mq, q, p, sd)) != FA_OK || (s = map16(&mk, k, p, sd)) != FA_OK ||
-      (s = map16(&mv, v, p, sd)) != FA_OK || (s = map16(&mo, o, p, sd)) != FA_OK)
+  if ((s = map16(&mq, q, p, p->H, sd)) != FA_OK || (s = map16(&mk, k, p, hkv, skv)) != FA_OK ||
+      (s = map16(&mv, v, p, hkv, skv)) != FA_OK || (s = map16(&mo, o, p, p->H, sd)) != FA_OK)
     return s;
   ProfScope prof(p, st);
   return cuda_status(launch_fwd_tc(p->dtype, mq, mk, mv, mo, a, st));
@@ -240,10 +266,13 @@ fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v
   if (ws == nullptr || ws_bytes < L.total || !aligned16(ws)) return FA_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  const Strides sd = strides_of(p);
+  const Strides sd = strides_of(p), skv = kv_strides_of(p);
+  const int hkv = hkv_of(p);
 
   BwdArgs a{};
   a.B = p->B; a.H = p->H; a.N = p->N;
+  a.group = p->H / hkv;
+  a.H_kv = hkv;
   a.nq = L.nq;
   a.npad = L.npad;
   a.scale = scale_of(p);
@@ -263,14 +292,14 @@ fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v
   if (p->dtype == FA_DT_F32) {
     ProfScope prof(p, st);
     return cuda_status(launch_bwd_simt((const float*)q, (const float*)k, (const float*)v, (const float*)dout,
-                                       (float*)dq, (float*)dk, (float*)dv, sd, a, st));
+                                       (float*)dq, (float*)dk, (float*)dv, sd, skv, a, st));
   }
   CUtensorMap mq, mk, mv, mdo, mdk, mdv, macc;
   Strides acc_st{(int64_t)p->H * p->N * kHeadDim, (int64_t)p->N * kHeadDim, kHeadDim};
-  if ((s = map16(&mq, q, p, sd)) != FA_OK || (s = map16(&mk, k, p, sd)) != FA_OK ||
-      (s = map16(&mv, v, p, sd)) != FA_OK || (s = map16(&mdo, dout, p, sd)) != FA_OK ||
-      (s = map16(&mdk, dk, p, sd)) != FA_OK || (s = map16(&mdv, dv, p, sd)) != FA_OK ||
-      (s = make_map(&macc, dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kHeadDim, 32, p, acc_st)) != FA_OK)
+  if ((s = map16(&mq, q, p, p->H, sd)) != FA_OK || (s = map16(&mk, k, p, hkv, skv)) != FA_OK ||
+      (s = map16(&mv, v, p, hkv, skv)) != FA_OK || (s = map16(&mdo, dout, p, p->H, sd)) != FA_OK ||
+      (s = map16(&mdk, dk, p, hkv, skv)) != FA_OK || (s = map16(&mdv, dv, p, hkv, skv)) != FA_OK ||
+      (s = make_map(&macc, dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kHeadDim, 32, p, p->H, acc_st)) != FA_OK)
     return s;
   {
     ProfScope prof(p, st);
@@ -313,6 +342,6 @@ const char* fa_status_string(fa_status s) {
   return "FA_ERR_UNKNOWN";
 }
 
-int32_t fa_version(void) { return 100; }
+int32_t fa_version(void) { return 101; }
 
 }  // extern "C"

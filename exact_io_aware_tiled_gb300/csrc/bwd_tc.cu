@@ -11,9 +11,16 @@
 //     dS^T = P^T o (dP^T - D_i)
 //     dV += P~^T dO_i,  dK += dS^T Q_i,  dQ_i += dS K      (tau applied at the end)
 //
-// GB300 mapping (ours): one CTA per (b, h, 128-key tile), looping over the
-// query tiles that see it; the CTAs of one head are adjacent in launch order
-// so its Q / dO tiles and dQ accumulator rows stay in L2.
+// Grouped-query attention (living-dl-book, "Atencao eficiente", section 6):
+// dK and dV of a K/V head shared by g query heads sum over those heads.  The
+// sliding window (lynx-cortex, "Problemas de practica") limits the query
+// tiles that see a key tile and masks the window's far edge.
+//
+// GB300 mapping (ours): one CTA per (b, K/V head, 128-key tile), looping over
+// the query tiles that see it for each query head of the group, so dK and dV
+// accumulate over the group in tensor memory; the CTAs of one head are
+// adjacent in launch order so its Q / dO tiles and dQ accumulator rows stay
+// in L2.
 //   * warp 16: TMA loads of K, V once and of Q_i, dO_i (+ LSE_i, D_i rows)
 //     into a three-stage ring;
 //   * three MMA-issuing warps (one thread each): consecutive MMAs into the
@@ -74,11 +81,14 @@ struct BBars {
 
 static_assert(sizeof(BBars) <= 256, "barrier block overflows its shared-memory slot");
 
+// The steps of one CTA: every query tile that sees its key tile, for each of
+// the g query heads that share its K/V head (head-major: step t is tile
+// t % n of query head h0 + t / n; the loops track both with counters).
 struct QList {
-  int n;
+  int n;                  // query tiles per query head
   int i0;                 // first query tile (dense)
+  int h0;                 // first query head of the group
   const int16_t* list;    // sparse list or nullptr
-  __device__ __forceinline__ int qt(int t) const { return list ? (int)list[t] : i0 + t; }
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
@@ -88,7 +98,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 constexpr uint32_t kColST = 0, kColDP = 128, kColDK = 256, kColDV = 320, kColDQ = 384, kColPT = 448;
 
-template <typename T, bool kDrop>
+template <typename T, bool kDrop, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -103,28 +113,35 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   // ---- work item: (b, h, key tile jt); the tiles of one head are adjacent,
   //      and under causal masking the longest query lists come first.
-  const int bh = (int)(blockIdx.x / a.nq);
+  const int bk = (int)(blockIdx.x / a.nq);
   const int jt = (int)(blockIdx.x % a.nq);
-  const int b = bh / a.H, h = bh % a.H;
+  const int b = bk / a.H_kv, hk = bk % a.H_kv;   // K/V head
   int Lk = a.N;
   if (a.mask.seqlens_k != nullptr) Lk = max(0, min(a.N, a.mask.seqlens_k[b]));
   QList ql;
   ql.list = nullptr;
   ql.i0 = a.mask.causal ? jt : 0;
+  ql.h0 = hk * a.group;
   ql.n = 0;
+  // last query tile that sees this key tile: under a sliding window of w keys,
+  // key j is seen by queries j .. j + w - 1
+  int qlast = a.nq - 1;
+  if (a.mask.window > 0) qlast = min(qlast, (jt * kTile + kTile - 1 + a.mask.window - 1) / kTile);
   if (jt * kTile < Lk) {
     if (a.mask.col_list != nullptr) {
-      ql.list = a.mask.col_list + (size_t)jt * a.mask.nb;
+      const int16_t* list = a.mask.col_list + (size_t)jt * a.mask.nb;
       const int cnt = a.mask.col_cnt[jt];
       int s0 = 0;
-      if (a.mask.causal) while (s0 < cnt && ql.list[s0] < jt) ++s0;
-      ql.list += s0;
-      ql.n = cnt - s0;
+      if (a.mask.causal) while (s0 < cnt && list[s0] < jt) ++s0;
+      int e = s0;
+      while (e < cnt && list[e] <= qlast) ++e;
+      ql.list = list + s0;
+      ql.n = e - s0;
     } else {
-      ql.n = a.nq - ql.i0;
+      ql.n = max(0, qlast - ql.i0 + 1);
     }
   }
-  const int n = ql.n;
+  const int n = ql.n * a.group;   // steps
   WaitCtl ctl{a.status, &bars->abort};
 
   if (threadIdx.x == 0) {
@@ -158,7 +175,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const size_t ld_row0 = (size_t)bh * a.npad;
 
   if (warp >= 16) {
     constexpr int ab = Cvt<T>::kAB;
@@ -174,19 +190,21 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmDO);
         mbar_expect_tx(&bars->kv_full, 32768);
-        tma_load_4d(smem + L::kK, &tmK, &bars->kv_full, 0, jt * kTile, h, b);
-        tma_load_4d(smem + L::kV, &tmV, &bars->kv_full, 0, jt * kTile, h, b);
+        tma_load_4d(smem + L::kK, &tmK, &bars->kv_full, 0, jt * kTile, hk, b);
+        tma_load_4d(smem + L::kV, &tmV, &bars->kv_full, 0, jt * kTile, hk, b);
         int issued = 0;
-        for (int t = 0; t < n; ++t) {
+        int qu = 0, hq = ql.h0;
+        for (int t = 0; t < n; ++t, qu = (qu + 1 == ql.n) ? 0 : qu + 1, hq += (qu == 0) ? 1 : 0) {
           const int st = t % NSB;
           const uint32_t ph = (uint32_t)(t / NSB) & 1u;
           if (!mbar_wait(&bars->q_empty[st], ph ^ 1u, ctl)) break;
-          const int qi = ql.qt(t);
+          const int qi = ql.list ? (int)ql.list[qu] : ql.i0 + qu;
+          const size_t ld_row = ((size_t)b * a.H + hq) * a.npad + (size_t)qi * kTile;
           mbar_expect_tx(&bars->q_full[st], 32768 + 1024);
-          tma_load_4d(smem + L::kQ + st * 16384, &tmQ, &bars->q_full[st], 0, qi * kTile, h, b);
-          tma_load_4d(smem + L::kDO + st * 16384, &tmDO, &bars->q_full[st], 0, qi * kTile, h, b);
-          bulk_load(smem + L::kLD + st * 1024, a.lse2 + ld_row0 + (size_t)qi * kTile, 512, &bars->q_full[st]);
-          bulk_load(smem + L::kLD + st * 1024 + 512, a.dvec + ld_row0 + (size_t)qi * kTile, 512, &bars->q_full[st]);
+          tma_load_4d(smem + L::kQ + st * 16384, &tmQ, &bars->q_full[st], 0, qi * kTile, hq, b);
+          tma_load_4d(smem + L::kDO + st * 16384, &tmDO, &bars->q_full[st], 0, qi * kTile, hq, b);
+          bulk_load(smem + L::kLD + st * 1024, a.lse2 + ld_row, 512, &bars->q_full[st]);
+          bulk_load(smem + L::kLD + st * 1024 + 512, a.dvec + ld_row, 512, &bars->q_full[st]);
           ++issued;
         }
         for (int t = max(0, issued - NSB); t < issued; ++t)
@@ -261,15 +279,18 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       // ===================== dQ issuer + dQ reduce =====================
       if (lane == 0 && n > 0) {
         prefetch_tmap(&tmDQ);
-        // staging buffer t % NSTG -> two TMA reduce-adds into the float32 accumulator
+        // staging buffer t % NSTG -> two TMA reduce-adds into the float32
+        // accumulator; called for t = 0, 1, ... in order (rqu / rhq follow t)
+        int rqu = 0, rhq = ql.h0;
         auto reduce = [&](int t) -> bool {
           const int bi = t % NSTG;
           if (!mbar_wait(&bars->stg_full[bi], (uint32_t)(t / NSTG) & 1u, ctl)) return false;
           const uint8_t* sb = smem + L::kDQ + bi * 32768;
-          const int qi = ql.qt(t);
-          tma_reduce_add_4d(&tmDQ, sb, 0, qi * kTile, h, b);
-          tma_reduce_add_4d(&tmDQ, sb + 16384, 32, qi * kTile, h, b);
+          const int qi = ql.list ? (int)ql.list[rqu] : ql.i0 + rqu;
+          tma_reduce_add_4d(&tmDQ, sb, 0, qi * kTile, rhq, b);
+          tma_reduce_add_4d(&tmDQ, sb + 16384, 32, qi * kTile, rhq, b);
           bulk_commit();
+          if (++rqu == ql.n) { rqu = 0; ++rhq; }
           bulk_wait_read0();
           mbar_arrive(&bars->stg_free[bi]);
           return true;
@@ -304,7 +325,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t tl = tmem + lane_off;
     const bool key_ok = j < Lk;
     const float sl2 = a.scale_log2;
-    const uint32_t bh_rows = (uint32_t)bh * (uint32_t)a.N;
     const int c0 = wg * 32;                   // first query column of this warpgroup
     // 16-byte pieces (w & 1) * 4 .. + 4 of a 128-byte swizzled row belong to this warpgroup
     const int pc_base = (wg & 1) * 4;
@@ -338,15 +358,20 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       return true;
     };
 
-    for (int t = 0; t < n && ok; ++t) {
+    // qu: tile position within the current query head qh (step t = (qh - h0) * ql.n + qu)
+    int qu = 0, qh = ql.h0;
+    for (int t = 0; t < n && ok; ++t, qu = (qu + 1 == ql.n) ? 0 : qu + 1, qh += (qu == 0) ? 1 : 0) {
       const int st = t % NSB;
-      const int qi = ql.qt(t);
+      const int qi = ql.list ? (int)ql.list[qu] : ql.i0 + qu;
+      const uint32_t bh_rows = ((uint32_t)b * (uint32_t)a.H + (uint32_t)qh) * (uint32_t)a.N;
       // LSE*log2e and D of this warpgroup's 32 query columns, in shared memory
       const uint32_t s_lse = smem_u32(smem + L::kLD + st * 1024) + c0 * 4;
       const uint32_t s_d = s_lse + 512;
-      // query column c (relative to c0) is hidden from this key under causal iff c0 + c < qlo
+      // query column c of the tile is hidden from this key under causal iff
+      // c < qlo, and outside its sliding window iff c >= qhe
       const int qlo = a.mask.causal ? (j - qi * kTile) : -1;
-      const bool any_mask = !key_ok || qlo > c0;
+      const int qhe = kWin ? (j + a.mask.window - qi * kTile) : kTile;
+      const bool any_mask = !key_ok || qlo > c0 || (kWin && qhe < c0 + 32);
 
       // ---- part 1: P from S^T, in two halves of 16 query columns; the
       //      tensor-memory load of the second half overlaps the first's math
@@ -386,7 +411,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           if (any_mask) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              if (!key_ok || c0 + cc + e < qlo) p[e] = 0.f;
+              if (!key_ok || c0 + cc + e < qlo || (kWin && c0 + cc + e >= qhe)) p[e] = 0.f;
           }
           const uint32_t w0 = Cvt<T>::pack(p[0], p[1]), w1 = Cvt<T>::pack(p[2], p[3]);
           pp[cc / 2] = w0;
@@ -501,8 +526,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       fence_proxy_async_smem();
       named_bar_sync(1, kCompute);
       if (threadIdx.x == 0) {
-        tma_store_4d(&tmDK, kb, 0, jt * kTile, h, b);
-        tma_store_4d(&tmDV, vb, 0, jt * kTile, h, b);
+        tma_store_4d(&tmDK, kb, 0, jt * kTile, hk, b);
+        tma_store_4d(&tmDV, vb, 0, jt * kTile, hk, b);
         bulk_commit();
         bulk_wait_read0();   // shared memory must outlive the reads; the writes finish with the grid
       }
@@ -517,14 +542,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
 }
 
-template <typename T, bool kDrop>
+template <typename T, bool kDrop, bool kWin>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
                      const CUtensorMap& dk, const CUtensorMap& dv, const CUtensorMap& dqacc, const BwdArgs& a,
                      cudaStream_t s) {
-  auto kern = bwd_tc_kernel<T, kDrop>;
+  auto kern = bwd_tc_kernel<T, kDrop, kWin>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem::kDyn);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(a.nq * a.B * a.H);
+  const unsigned grid = (unsigned)(a.nq * a.B * a.H_kv);
   if (grid == 0) return cudaSuccess;
   kern<<<grid, kThreads, BwdSmem::kDyn, s>>>(q, k, v, dout, dk, dv, dqacc, a);
   return cudaGetLastError();
@@ -535,12 +560,22 @@ cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
 cudaError_t launch_bwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
                           const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s) {
-  const bool d = a.drop.enabled != 0;
-  if (dtype == FA_DT_BF16)
-    return d ? launch_t<__nv_bfloat16, true>(q, k, v, dout, dk, dv, dqacc, a, s)
-             : launch_t<__nv_bfloat16, false>(q, k, v, dout, dk, dv, dqacc, a, s);
-  return d ? launch_t<__half, true>(q, k, v, dout, dk, dv, dqacc, a, s)
-           : launch_t<__half, false>(q, k, v, dout, dk, dv, dqacc, a, s);
+  const int sel = (a.drop.enabled ? 1 : 0) | (a.mask.window > 0 ? 2 : 0);
+  if (dtype == FA_DT_BF16) {
+    using B = __nv_bfloat16;
+    switch (sel) {
+      case 0: return launch_t<B, false, false>(q, k, v, dout, dk, dv, dqacc, a, s);
+      case 1: return launch_t<B, true, false>(q, k, v, dout, dk, dv, dqacc, a, s);
+      case 2: return launch_t<B, false, true>(q, k, v, dout, dk, dv, dqacc, a, s);
+      default: return launch_t<B, true, true>(q, k, v, dout, dk, dv, dqacc, a, s);
+    }
+  }
+  switch (sel) {
+    case 0: return launch_t<__half, false, false>(q, k, v, dout, dk, dv, dqacc, a, s);
+    case 1: return launch_t<__half, true, false>(q, k, v, dout, dk, dv, dqacc, a, s);
+    case 2: return launch_t<__half, false, true>(q, k, v, dout, dk, dv, dqacc, a, s);
+    default: return launch_t<__half, true, true>(q, k, v, dout, dk, dv, dqacc, a, s);
+  }
 }
 
 }  // namespace fa

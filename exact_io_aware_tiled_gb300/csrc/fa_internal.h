@@ -25,6 +25,7 @@ struct DropoutArgs {
 
 struct MaskArgs {
   int causal;
+  int window;                 // sliding window w (causal only), 0 = none
   const int32_t* seqlens_k;   // device [B] or nullptr
   const int16_t* row_list;    // [nb][nb]: kept kv tiles of each q tile, ascending
   const int32_t* row_cnt;     // [nb]
@@ -35,6 +36,7 @@ struct MaskArgs {
 
 struct FwdArgs {
   int B, H, N;
+  int group;                  // query heads per K/V head (H / H_kv)
   int nq;                     // ceil(N / 128)
   int npairs;                 // ceil(nq / 2)
   float scale_log2;           // tau * log2(e)
@@ -47,6 +49,8 @@ struct FwdArgs {
 
 struct BwdArgs {
   int B, H, N;
+  int group;                  // query heads per K/V head (H / H_kv)
+  int H_kv;
   int nq;                     // ceil(N / 128)
   int npad;                   // nq * 128
   float scale;                // tau
@@ -69,10 +73,11 @@ cudaError_t launch_bwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k,
 
 struct Strides { int64_t b, h, n; };
 
+// st: strides of Q, O, dO, dQ ([B,H,N,d]); kst: strides of K, V, dK, dV ([B,H_kv,N,d]).
 cudaError_t launch_fwd_simt(const float* q, const float* k, const float* v, float* o, Strides st,
-                            const FwdArgs& a, cudaStream_t s);
+                            Strides kst, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_simt(const float* q, const float* k, const float* v, const float* dout,
-                            float* dq, float* dk, float* dv, Strides st, const BwdArgs& a,
+                            float* dq, float* dk, float* dv, Strides st, Strides kst, const BwdArgs& a,
                             cudaStream_t s);
 
 // D = rowsum(dO o O) and the padded LSE*log2e / D arrays; zeroes dqacc if given.

@@ -9,6 +9,11 @@
 // (agihunt.info, fused-kernel paragraph).  Only O and the per-row
 // logsumexp leave the chip.
 //
+// Grouped-query attention (living-dl-book, "Atencao eficiente", section 6):
+// query head h reads K/V head h / g.  Sliding window (lynx-cortex, "Problemas
+// de practica"): a query tile reads only the K/V tiles its rows' windows
+// reach, and the window's lower edge is masked like the causal upper edge.
+//
 // GB300 mapping (ours, not the pages'):
 //   * one CTA = two 128-row query tiles ("slots") of one (b, h) head;
 //   * warp 8 (one thread) streams K/V tiles with TMA into a ring of NS
@@ -64,8 +69,9 @@ struct Bars {
 struct Slot {
   int qt;                 // query tile index
   int n;                  // kv steps
+  int lo;                 // first kv tile (dense)
   const int16_t* list;    // sparse kv list or nullptr
-  __device__ __forceinline__ int kv(int s) const { return list ? (int)list[s] : s; }
+  __device__ __forceinline__ int kv(int s) const { return list ? (int)list[s] : lo + s; }
 };
 
 __device__ __forceinline__ Slot make_slot(const FwdArgs& a, int qt, int Lk) {
@@ -73,17 +79,23 @@ __device__ __forceinline__ Slot make_slot(const FwdArgs& a, int qt, int Lk) {
   sl.qt = qt;
   sl.list = nullptr;
   sl.n = 0;
+  sl.lo = 0;
   if (qt >= a.nq) return sl;
   int lim = (Lk + kTile - 1) / kTile;
   if (a.mask.causal) lim = min(lim, qt + 1);
+  // sliding window: the tile's first query sees keys from qt*128 - w + 1 on
+  if (a.mask.window > 0) sl.lo = max(0, qt * kTile - a.mask.window + 1) / kTile;
   if (a.mask.row_list != nullptr) {
-    sl.list = a.mask.row_list + (size_t)qt * a.mask.nb;
+    const int16_t* list = a.mask.row_list + (size_t)qt * a.mask.nb;
     const int cnt = a.mask.row_cnt[qt];
-    int n = 0;
-    while (n < cnt && sl.list[n] < lim) ++n;
-    sl.n = n;
+    int s0 = 0;
+    while (s0 < cnt && list[s0] < sl.lo) ++s0;
+    int n = s0;
+    while (n < cnt && list[n] < lim) ++n;
+    sl.list = list + s0;
+    sl.n = n - s0;
   } else {
-    sl.n = lim;
+    sl.n = max(0, lim - sl.lo);
   }
   return sl;
 }
@@ -125,7 +137,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-template <typename T, bool kDrop>
+template <typename T, bool kDrop, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -143,6 +155,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const int pair = a.npairs - 1 - (int)(blockIdx.x / BH);
   const int bh = (int)(blockIdx.x % BH);
   const int b = bh / a.H, h = bh % a.H;
+  const int hk = h / a.group;            // K/V head shared by this query head's group
   int Lk = a.N;
   if (a.mask.seqlens_k != nullptr) Lk = max(0, min(a.N, a.mask.seqlens_k[b]));
   Slot sl[2];
@@ -207,9 +220,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                      mbar_wait(&bars->v_empty[st], p.ph[l] ^ 1u, ctl)))
             break;
           mbar_expect_tx(&bars->k_full[st], 16384);
-          tma_load_4d(smem + C::kK + st * 16384, &tmK, &bars->k_full[st], 0, p.kv[l] * kTile, h, b);
+          tma_load_4d(smem + C::kK + st * 16384, &tmK, &bars->k_full[st], 0, p.kv[l] * kTile, hk, b);
           mbar_expect_tx(&bars->v_full[st], 16384);
-          tma_load_4d(smem + C::kV + st * 16384, &tmV, &bars->v_full[st], 0, p.kv[l] * kTile, h, b);
+          tma_load_4d(smem + C::kV + st * 16384, &tmV, &bars->v_full[st], 0, p.kv[l] * kTile, hk, b);
         }
       }
       // Before leaving, make sure no load is still writing shared memory.
@@ -299,6 +312,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t tS = tmem + x * 256 + lane_off, tP = tS + 128, tO = tS + 192;
     const float sl2 = a.scale_log2;
     const int jmax = a.mask.causal ? min(Lk - 1, i) : (Lk - 1);
+    const int jmin = kWin ? i - a.mask.window + 1 : 0;   // first key of the sliding window
     const uint32_t row_g = (uint32_t)(b * a.H + h) * (uint32_t)a.N + (uint32_t)i;
 
     float m_run = -INFINITY;
@@ -319,10 +333,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
       // mask (only boundary tiles) and row max of the raw scores
       const int jl = jmax - kv * kTile;
-      if (jl < kTile - 1) {
+      const int jlo = jmin - kv * kTile;
+      if (jl < kTile - 1 || (kWin && jlo > 0)) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (c > jl) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          if (c > jl || (kWin && c < jlo)) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
       // row max: 8 independent chains of 3-input max, then a short tree
       float m8[8];
@@ -471,10 +486,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
 }
 
-template <typename T, bool kDrop>
+template <typename T, bool kDrop, bool kWin>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
                      const FwdArgs& a, cudaStream_t s) {
-  auto kern = fwd_tc_kernel<T, kDrop>;
+  auto kern = fwd_tc_kernel<T, kDrop, kWin>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg::kDyn);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(a.npairs * a.B * a.H);
@@ -487,10 +502,22 @@ cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
 
 cudaError_t launch_fwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& o, const FwdArgs& a, cudaStream_t s) {
-  const bool d = a.drop.enabled != 0;
-  if (dtype == FA_DT_BF16)
-    return d ? launch_t<__nv_bfloat16, true>(q, k, v, o, a, s) : launch_t<__nv_bfloat16, false>(q, k, v, o, a, s);
-  return d ? launch_t<__half, true>(q, k, v, o, a, s) : launch_t<__half, false>(q, k, v, o, a, s);
+  const int sel = (a.drop.enabled ? 1 : 0) | (a.mask.window > 0 ? 2 : 0);
+  if (dtype == FA_DT_BF16) {
+    using B = __nv_bfloat16;
+    switch (sel) {
+      case 0: return launch_t<B, false, false>(q, k, v, o, a, s);
+      case 1: return launch_t<B, true, false>(q, k, v, o, a, s);
+      case 2: return launch_t<B, false, true>(q, k, v, o, a, s);
+      default: return launch_t<B, true, true>(q, k, v, o, a, s);
+    }
+  }
+  switch (sel) {
+    case 0: return launch_t<__half, false, false>(q, k, v, o, a, s);
+    case 1: return launch_t<__half, true, false>(q, k, v, o, a, s);
+    case 2: return launch_t<__half, false, true>(q, k, v, o, a, s);
+    default: return launch_t<__half, true, true>(q, k, v, o, a, s);
+  }
 }
 
 }  // namespace fa

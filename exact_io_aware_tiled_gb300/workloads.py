@@ -18,7 +18,9 @@ block-sparse paragraph):
   to the storage dtype with round-to-nearest-even (torch CPU casts);
 * key-padding lengths L_b = integers(lo, hi + 1) from stream 4;
 * block-sparse: kept(I, J) iff I == J or I ^ J is a power of two over
-  N / 128 blocks.
+  N / 128 blocks;
+* grouped-query: K and V are drawn with ``H_kv`` heads ([B, H_kv, N, d]);
+* the sliding window is a mask parameter (``window``) and draws nothing.
 """
 from __future__ import annotations
 
@@ -57,6 +59,8 @@ class Workload:
     seed: int = 20260
     seqlens: Optional[np.ndarray] = field(default=None, repr=False)
     block_mask: Optional[np.ndarray] = field(default=None, repr=False)
+    H_kv: Optional[int] = None                # K/V heads (grouped-query); None -> H
+    window: int = 0                           # causal sliding window of keys (0 = none)
 
     def __post_init__(self):
         if self.seqlen_range is not None and self.seqlens is None:
@@ -71,6 +75,10 @@ class Workload:
     def torch_dtype(self):
         return DTYPES[self.dtype]
 
+    @property
+    def hkv(self) -> int:
+        return self.H if self.H_kv is None else int(self.H_kv)
+
     def with_(self, **kw):
         return replace(self, **kw)
 
@@ -84,9 +92,10 @@ def _draw(shape, seed, stream, scale, dtype):
 
 
 def make_inputs(wl: Workload, grads: bool = True):
-    """q, k, v (and do) as torch CPU tensors of the storage dtype, [B,H,N,d]."""
+    """q, do as [B,H,N,d] and k, v as [B,H_kv,N,d] torch CPU tensors of the storage dtype."""
     shp = (wl.B, wl.H, wl.N, wl.d)
-    out = {n: _draw(shp, wl.seed, s, wl.input_scale, wl.dtype)
+    kshp = (wl.B, wl.hkv, wl.N, wl.d)
+    out = {n: _draw(shp if n == "q" else kshp, wl.seed, s, wl.input_scale, wl.dtype)
            for s, n in enumerate(("q", "k", "v"))}
     if grads:
         out["do"] = _draw(shp, wl.seed, 3, wl.input_scale, wl.dtype)

@@ -20,10 +20,22 @@
  *     Q-outer loop with deferred normalisation used by the forward kernel).
  *
  * Conventions shared by every entry point
- *   - Tensors Q, K, V, O, dO, dQ, dK, dV are logical [B, H, N, d] arrays of
- *     one dtype, addressed as base + b*stride_b + h*stride_h + n*stride_n + c
- *     (element strides; the head dimension is contiguous).  LSE is a
- *     contiguous float32 [B, H, N] array.
+ *   - Tensors Q, O, dO, dQ are logical [B, H, N, d] arrays of one dtype,
+ *     addressed as base + b*stride_b + h*stride_h + n*stride_n + c (element
+ *     strides; the head dimension is contiguous).  K, V, dK, dV are
+ *     [B, H_kv, N, d] arrays of the same dtype with the kv_stride_* strides;
+ *     H_kv = H (multi-head attention) unless grouped-query attention is asked
+ *     for.  LSE is a contiguous float32 [B, H, N] array.
+ *   - Grouped-query attention (living-dl-book, "Atencao eficiente", section
+ *     6): the H query heads form H_kv groups of g = H / H_kv heads, and every
+ *     head of group k reads K/V head k, i.e. query head h reads K/V head h / g;
+ *     g = 1 is multi-head and g = H multi-query attention.  dK and dV of a
+ *     shared head are the sums over its g query heads.
+ *   - Sliding window (lynx-cortex, "Problemas de practica", the
+ *     sliding-window exercise), read as the local causal window: with
+ *     window = w > 0 and causal set, key j is visible to query i iff
+ *     i - w < j <= i; whole K/V tiles outside every window of a query tile
+ *     are skipped.
  *   - Ownership: the caller owns every buffer and the stream.  The library
  *     never allocates, frees or synchronises device memory, except that
  *     fa_check_status synchronises the stream it is given.  Work is enqueued
@@ -83,6 +95,13 @@ typedef struct {
   void *prof_stop;           /* they are recorded on `stream` right before and
                                 right after the main attention kernel of the
                                 call (profiling; not owned by the library)      */
+  /* -- ABI 1.1 -- zero-filled by callers of 1.0, which keeps their meaning */
+  int32_t H_kv;              /* K/V heads; H % H_kv == 0; 0 selects H           */
+  int64_t kv_stride_b;       /* element strides of K, V, dK, dV [B,H_kv,N,d];   */
+  int64_t kv_stride_h;       /* all three 0 selects stride_b/h/n, allowed only  */
+  int64_t kv_stride_n;       /* when H_kv == H                                  */
+  int32_t window;            /* w > 0: key j visible to query i only if
+                                i - w < j (requires causal); 0 = no window     */
 } fa_params;
 
 /* ---------------------------------------------------------------------------
@@ -182,7 +201,8 @@ fa_status fa_dropout_mask(const fa_params *p, int32_t b, int32_t h, int32_t row0
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *fa_status_string(fa_status s);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor): 101 adds H_kv, kv_stride_*
+ * and window to fa_params. */
 int32_t fa_version(void);
 
 #ifdef __cplusplus

@@ -21,6 +21,8 @@ the gradient would have without that cancellation:
   floor(dQ) = 0.1 tau ||dO||_F rms_j||V_j|| rms_j||K_j||,
   floor(dK) = 0.1 tau ||dO||_F rms_j||V_j|| rms_i||Q_i||,
   floor(dV) = 0.1 ||dO||_F.
+For a K/V head shared by g query heads (grouped-query attention) dK and dV
+sum over the group, and so do their floors, in quadrature.
 """
 from __future__ import annotations
 
@@ -53,14 +55,15 @@ def spec_of(wl: W.Workload) -> A.Spec:
                   seqlens_k=None if wl.seqlens is None else np.asarray(wl.seqlens),
                   block_mask=None if wl.block_mask is None else wl.block_mask.astype(bool),
                   block_size=wl.block_size, dropout_p=wl.dropout_p, seed=wl.dropout_seed,
-                  offset=wl.dropout_offset)
+                  offset=wl.dropout_offset, H_kv=wl.H_kv, window=wl.window)
 
 
 def kwargs_of(wl: W.Workload):
     return dict(causal=wl.causal,
                 seqlens_k=None if wl.seqlens is None else torch.from_numpy(np.asarray(wl.seqlens, dtype=np.int32)),
                 dropout_p=wl.dropout_p, seed=wl.dropout_seed, offset=wl.dropout_offset,
-                block_mask=None if wl.block_mask is None else torch.from_numpy(wl.block_mask.astype(np.uint8)))
+                block_mask=None if wl.block_mask is None else torch.from_numpy(wl.block_mask.astype(np.uint8)),
+                window=wl.window)
 
 
 def run_gpu(wl: W.Workload, inputs, layout="bhnd", want_o32=True):
@@ -106,10 +109,17 @@ def _rms_row(x):
 
 
 def check_head(wl, inputs, got, b, h, rows=None, cols=None, do_grads=True):
-    """Compare one head (optionally sampled rows / cols) with the oracle."""
+    """Compare query head h of batch b (optionally sampled rows / cols) with the oracle.
+
+    O, LSE and dQ are checked for head h.  dK and dV belong to K/V head
+    h // g and sum over the g query heads of its group; they are checked when
+    h is the last head of its group (every head when g = 1)."""
     spec = spec_of(wl)
     tol = TOL[wl.dtype]
-    q, k, v = (np64(inputs[n][b, h]) for n in ("q", "k", "v"))
+    g = spec.group
+    hk = h // g
+    q = np64(inputs["q"][b, h])
+    k, v = np64(inputs["k"][b, hk]), np64(inputs["v"][b, hk])
     rr = np.arange(wl.N) if rows is None else np.asarray(rows)
     cc = np.arange(wl.N) if cols is None else np.asarray(cols)
     O, L = A.head_forward(spec, b, h, q, k, v, rows=rr)
@@ -140,15 +150,26 @@ def check_head(wl, inputs, got, b, h, rows=None, cols=None, do_grads=True):
         assert report["o_stored_excess"] <= 0.0, report
     if do_grads and "dq" in got:
         do = np64(inputs["do"][b, h])
-        g = A.head_backward(spec, b, h, q, k, v, do, rows=rr, cols=cc)
+        gr = A.head_backward(spec, b, h, q, k, v, do, rows=rr, cols=cc)
         ndo = float(np.linalg.norm(do))
-        fl = {"dq": 0.1 * spec.tau * ndo * _rms_row(v) * _rms_row(k),
-              "dk": 0.1 * spec.tau * ndo * _rms_row(v) * _rms_row(q),
-              "dv": 0.1 * ndo}
-        for name, ref, gg in (("dq", g["dq"], sel("dq", rr_t)), ("dk", g["dk"], sel("dk", cc_t)),
-                              ("dv", g["dv"], sel("dv", cc_t))):
-            report[name] = rel_frob(gg, ref, fl[name])
-            assert report[name] <= tol["grad"], (name, report)
+        fl = 0.1 * spec.tau * ndo * _rms_row(v) * _rms_row(k)
+        report["dq"] = rel_frob(sel("dq", rr_t), gr["dq"], fl)
+        assert report["dq"] <= tol["grad"], ("dq", report)
+        if h % g == g - 1:
+            dk_ref, dv_ref = np.zeros((cc.size, spec.d)), np.zeros((cc.size, spec.d))
+            fk2 = fv2 = 0.0
+            for hq in range(hk * g, hk * g + g):
+                qh, doh = np64(inputs["q"][b, hq]), np64(inputs["do"][b, hq])
+                gh = gr if hq == h else A.head_backward(spec, b, hq, qh, k, v, doh, rows=np.arange(0), cols=cc)
+                dk_ref += gh["dk"]
+                dv_ref += gh["dv"]
+                nd = float(np.linalg.norm(doh))
+                fk2 += (0.1 * spec.tau * nd * _rms_row(v) * _rms_row(qh)) ** 2
+                fv2 += (0.1 * nd) ** 2
+            sel_kv = lambda name: _np(got[name][b, hk][cc_t.to(got[name].device)])
+            for name, ref, floor in (("dk", dk_ref, fk2 ** 0.5), ("dv", dv_ref, fv2 ** 0.5)):
+                report[name] = rel_frob(sel_kv(name), ref, floor)
+                assert report[name] <= tol["grad"], (name, report)
     return report
 
 

@@ -78,7 +78,7 @@ def _params(**kw):
 def test_status_strings(lib):
     assert lib.fa_status_string(0) == b"FA_OK"
     assert lib.fa_status_string(6) == b"FA_ERR_TIMEOUT"
-    assert lib.fa_version() >= 100
+    assert lib.fa_version() >= 101
 
 
 def test_workspace_sizes(lib):
@@ -104,6 +104,11 @@ FAKE = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: validation fail
     (dict(dropout_p=1.0), 1),
     (dict(dropout_p=-0.1), 1),
     (dict(block_mask=1 << 20, block_size=64), 2),
+    (dict(H_kv=2), 1),                # 3 query heads cannot share 2 K/V heads
+    (dict(H_kv=1), 1),                # fewer K/V heads need their own strides
+    (dict(H_kv=1, kv_stride_b=200 * 64, kv_stride_h=200 * 64, kv_stride_n=68), 3),
+    (dict(window=5), 2),              # a sliding window needs causal masking
+    (dict(window=-1, causal=1), 1),
 ])
 def test_host_validation_rejects_before_launch(lib, mut, code):
     p = _params(**mut)

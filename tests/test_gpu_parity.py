@@ -109,3 +109,39 @@ def test_host_errors_are_raised_not_hidden():
     q = torch.zeros((1, 1, 64, 128), device="cuda", dtype=torch.bfloat16)
     with pytest.raises(fa.FAError):
         fa.fwd(q, q, q)
+
+
+# ---- grouped-query attention (living-dl-book, efficient attention, section 6)
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("H,H_kv", [(4, 2), (3, 1)])
+def test_grouped_query(dtype, H, H_kv):
+    _check_all_heads(_wl(300, dtype, B=2, H=H, H_kv=H_kv, causal=True))
+
+
+def test_grouped_query_dense_dropout_padding_and_strides():
+    wl = _wl(257, "bf16", B=2, H=4, H_kv=2, dropout_p=0.2, seqlens=np.array([0, 200], dtype=np.int32))
+    _check_all_heads(wl)
+    _check_all_heads(wl.with_(dropout_p=0.0), layout="bnhd")
+
+
+# ---- causal sliding window (lynx-cortex, "Problemas de practica")
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("w", [1, 64, 128, 129, 300, 2000])
+def test_sliding_window(dtype, w):
+    _check_all_heads(_wl(513, dtype, B=1, H=2, causal=True, window=w))
+
+
+def test_sliding_window_with_groups_padding_dropout():
+    wl = _wl(384, "bf16", B=2, H=4, H_kv=2, causal=True, window=150, dropout_p=0.2,
+             seqlens=np.array([200, 384], dtype=np.int32))
+    _check_all_heads(wl)
+
+
+def test_sliding_window_with_block_sparse():
+    _check_all_heads(_wl(1024, "bf16", B=1, H=2, sparse_butterfly=True, causal=True, window=300))
+
+
+def test_sliding_window_requires_causal():
+    q = torch.zeros((1, 1, 128, 64), device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(fa.FAError):
+        fa.fwd(q, q, q, window=16)
