@@ -22,7 +22,8 @@
 // adjacent in launch order so its Q / dO tiles and dQ accumulator rows stay
 // in L2.
 //   * warp 16: TMA loads of K, V once and of Q_i, dO_i (+ LSE_i, D_i rows)
-//     into a three-stage ring;
+//     into a three-stage ring, and the two TMA reduce-adds of each staged
+//     dQ_i into the float32 accumulator;
 //   * three MMA-issuing warps (one thread each): consecutive MMAs into the
 //     same accumulator complete about 126 cycles apart whatever their N, so
 //     each product is a latency chain, and independent chains are issued
@@ -31,9 +32,7 @@
 //                as soon as the softmax warps have read the previous one;
 //       warp 18: dV += P~^T dO_i (A from tensor memory) and
 //                dK += dS^T Q_i (A from the shared dS^T tile);
-//       warp 19: dQ_i = dS K (A = the same tile read MN-major), then the two
-//                TMA reduce-adds of the staged dQ_{i-1} into the float32
-//                accumulator;
+//       warp 19: dQ_i = dS K (A = the same tile read MN-major);
 //   * warps 0-15: four warpgroups, each owning 32 of the 128 query columns
 //     of every key row (= tensor-memory lane):
 //       part 1: P from S^T, P~^T (16 bit) into tensor memory for dV;
@@ -185,31 +184,59 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
     const uint32_t sDS = smem_u32(smem + L::kDS);
     if (warp == 16) {
-      // ===================== TMA producer =====================
+      // ===================== TMA producer + dQ reduce =====================
+      // Loads of step t and the reduce of the staged dQ of step t - kLag run
+      // interleaved in one thread: the reduce of step r can only be staged
+      // after the load of step r + 1, and the load of step t needs, through
+      // the compute chain, the reduce of step t - 6, so this order never
+      // waits on itself; with the ring three steps deep each wait falls due
+      // at about the time the thread reaches it.
       if (lane == 0 && n > 0) {
+        constexpr int kLag = 3;
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmDO);
+        prefetch_tmap(&tmDQ);
         mbar_expect_tx(&bars->kv_full, 32768);
         tma_load_4d(smem + L::kK, &tmK, &bars->kv_full, 0, jt * kTile, hk, b);
         tma_load_4d(smem + L::kV, &tmV, &bars->kv_full, 0, jt * kTile, hk, b);
         int issued = 0;
-        int qu = 0, hq = ql.h0;
-        for (int t = 0; t < n; ++t, qu = (qu + 1 == ql.n) ? 0 : qu + 1, hq += (qu == 0) ? 1 : 0) {
-          const int st = t % NSB;
-          const uint32_t ph = (uint32_t)(t / NSB) & 1u;
-          if (!mbar_wait(&bars->q_empty[st], ph ^ 1u, ctl)) break;
-          const int qi = ql.list ? (int)ql.list[qu] : ql.i0 + qu;
-          const size_t ld_row = ((size_t)b * a.H + hq) * a.npad + (size_t)qi * kTile;
-          mbar_expect_tx(&bars->q_full[st], 32768 + 1024);
-          tma_load_4d(smem + L::kQ + st * 16384, &tmQ, &bars->q_full[st], 0, qi * kTile, hq, b);
-          tma_load_4d(smem + L::kDO + st * 16384, &tmDO, &bars->q_full[st], 0, qi * kTile, hq, b);
-          bulk_load(smem + L::kLD + st * 1024, a.lse2 + ld_row, 512, &bars->q_full[st]);
-          bulk_load(smem + L::kLD + st * 1024 + 512, a.dvec + ld_row, 512, &bars->q_full[st]);
-          ++issued;
+        bool ok = true;
+        int qu = 0, hq = ql.h0;      // load side: tile within query head hq
+        int rqu = 0, rhq = ql.h0;    // reduce side
+        for (int t = 0; t < n + kLag && ok; ++t) {
+          if (t < n) {
+            const int st = t % NSB;
+            const uint32_t ph = (uint32_t)(t / NSB) & 1u;
+            if (!(ok = mbar_wait(&bars->q_empty[st], ph ^ 1u, ctl))) break;
+            const int qi = ql.list ? (int)ql.list[qu] : ql.i0 + qu;
+            const size_t ld_row = ((size_t)b * a.H + hq) * a.npad + (size_t)qi * kTile;
+            mbar_expect_tx(&bars->q_full[st], 32768 + 1024);
+            tma_load_4d(smem + L::kQ + st * 16384, &tmQ, &bars->q_full[st], 0, qi * kTile, hq, b);
+            tma_load_4d(smem + L::kDO + st * 16384, &tmDO, &bars->q_full[st], 0, qi * kTile, hq, b);
+            bulk_load(smem + L::kLD + st * 1024, a.lse2 + ld_row, 512, &bars->q_full[st]);
+            bulk_load(smem + L::kLD + st * 1024 + 512, a.dvec + ld_row, 512, &bars->q_full[st]);
+            ++issued;
+            if (++qu == ql.n) { qu = 0; ++hq; }
+          }
+          const int r = t - kLag;
+          if (r >= 0 && r < n) {
+            // staging buffer r % NSTG -> two TMA reduce-adds into the float32 accumulator
+            const int bi = r % NSTG;
+            if (!(ok = mbar_wait(&bars->stg_full[bi], (uint32_t)(r / NSTG) & 1u, ctl))) break;
+            const uint8_t* sb = smem + L::kDQ + bi * 32768;
+            const int qi = ql.list ? (int)ql.list[rqu] : ql.i0 + rqu;
+            tma_reduce_add_4d(&tmDQ, sb, 0, qi * kTile, rhq, b);
+            tma_reduce_add_4d(&tmDQ, sb + 16384, 32, qi * kTile, rhq, b);
+            bulk_commit();
+            if (++rqu == ql.n) { rqu = 0; ++rhq; }
+            bulk_wait_read0();
+            mbar_arrive(&bars->stg_free[bi]);
+          }
         }
         for (int t = max(0, issued - NSB); t < issued; ++t)
           mbar_wait(&bars->q_full[t % NSB], (uint32_t)(t / NSB) & 1u, ctl);
         mbar_wait(&bars->kv_full, 0, ctl);
+        bulk_wait_read0();
       }
     } else if (warp == 17) {
       // ===================== S^T / dP^T issuer =====================
@@ -276,25 +303,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_wait(&bars->done[1], 0, ctl);
       }
     } else {
-      // ===================== dQ issuer + dQ reduce =====================
+      // ===================== dQ issuer (warp 19) =====================
       if (lane == 0 && n > 0) {
-        prefetch_tmap(&tmDQ);
-        // staging buffer t % NSTG -> two TMA reduce-adds into the float32
-        // accumulator; called for t = 0, 1, ... in order (rqu / rhq follow t)
-        int rqu = 0, rhq = ql.h0;
-        auto reduce = [&](int t) -> bool {
-          const int bi = t % NSTG;
-          if (!mbar_wait(&bars->stg_full[bi], (uint32_t)(t / NSTG) & 1u, ctl)) return false;
-          const uint8_t* sb = smem + L::kDQ + bi * 32768;
-          const int qi = ql.list ? (int)ql.list[rqu] : ql.i0 + rqu;
-          tma_reduce_add_4d(&tmDQ, sb, 0, qi * kTile, rhq, b);
-          tma_reduce_add_4d(&tmDQ, sb + 16384, 32, qi * kTile, rhq, b);
-          bulk_commit();
-          if (++rqu == ql.n) { rqu = 0; ++rhq; }
-          bulk_wait_read0();
-          mbar_arrive(&bars->stg_free[bi]);
-          return true;
-        };
         bool ok = true;
         for (int t = 0; t < n && ok; ++t) {
           // dQ_t = dS K  (M = 128 queries from the MN-major view of dS^T, K-dim = 128 keys)
@@ -307,12 +317,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                    idQ, k > 0 ? 1u : 0u);
           mma_commit(&bars->dq_full);
           mma_commit(&bars->dsm_free);
-          if (t > 0) ok = reduce(t - 1);
         }
-        if (ok) reduce(n - 1);
         mma_commit(&bars->done[2]);
         mbar_wait(&bars->done[2], 0, ctl);
-        bulk_wait_read0();
       }
     }
   } else {
@@ -331,7 +338,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     bool ok = true;
 
     // dQ_t: 16 of its 64 columns, tensor memory -> x tau -> staging buffer t % NSTG
-    // (warp 18 reduces it)
+    // (warp 16 reduces it)
     auto drain_dq = [&](int t) -> bool {
       if (!warp_wait(&bars->dq_full, (uint32_t)t & 1u, ctl)) return false;
       tc_fence_after();

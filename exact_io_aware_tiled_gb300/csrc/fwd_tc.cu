@@ -71,7 +71,9 @@ struct Slot {
   int n;                  // kv steps
   int lo;                 // first kv tile (dense)
   const int16_t* list;    // sparse kv list or nullptr
-  __device__ __forceinline__ int kv(int s) const { return list ? (int)list[s] : lo + s; }
+  // kv tile of step s (lo is nonzero only under a sliding window)
+  template <bool kWin>
+  __device__ __forceinline__ int kv(int s) const { return list ? (int)list[s] : (kWin ? lo + s : s); }
 };
 
 __device__ __forceinline__ Slot make_slot(const FwdArgs& a, int qt, int Lk) {
@@ -111,12 +113,13 @@ struct StepPlan {
   int use[2];             // load index used by slot x, or -1
 };
 
+template <bool kWin>
 __device__ __forceinline__ StepPlan plan_step(const Slot (&sl)[2], int s, int& ld) {
   StepPlan p;
   p.nl = 0;
   p.use[0] = p.use[1] = -1;
-  const int kvA = s < sl[0].n ? sl[0].kv(s) : -1;
-  const int kvB = s < sl[1].n ? sl[1].kv(s) : -1;
+  const int kvA = s < sl[0].n ? sl[0].kv<kWin>(s) : -1;
+  const int kvB = s < sl[1].n ? sl[1].kv<kWin>(s) : -1;
   if (kvA >= 0) {
     p.st[0] = ld % NS; p.ph[0] = (uint32_t)(ld / NS) & 1u; p.kv[0] = kvA; ++ld;
     p.use[0] = 0; p.nl = 1;
@@ -213,7 +216,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       int ld = 0;
       bool ok = true;
       for (int s = 0; s < smax && ok; ++s) {
-        const StepPlan p = plan_step(sl, s, ld);
+        const StepPlan p = plan_step<kWin>(sl, s, ld);
         for (int l = 0; l < p.nl; ++l) {
           const int st = p.st[l];
           if (!(ok = mbar_wait(&bars->k_empty[st], p.ph[l] ^ 1u, ctl) &&
@@ -242,7 +245,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       bool ok = mbar_wait(&bars->q_full, 0, ctl);
       int ld = 0;
       for (int s = 0; s < smax && ok; ++s) {
-        const StepPlan p = plan_step(sl, s, ld);
+        const StepPlan p = plan_step<kWin>(sl, s, ld);
         for (int x = 0; x < 2 && ok; ++x) {
           if (s >= sl[x].n) continue;
           const int l = p.use[x];
@@ -271,7 +274,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       int ld = 0;
       bool ok = true;
       for (int s = 0; s < smax && ok; ++s) {
-        const StepPlan p = plan_step(sl, s, ld);
+        const StepPlan p = plan_step<kWin>(sl, s, ld);
         if (s < n) {
           const int l = p.use[x];
           const int st = p.st[l];
@@ -319,7 +322,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     float l_true = 0.f, l_rnd = 0.f;
     bool ok = true;
     for (int s = 0; s < S.n; ++s) {
-      const int kv = S.kv(s);
+      const int kv = S.kv<kWin>(s);
       if (!(ok = warp_wait(&bars->s_full[x], (uint32_t)s & 1u, ctl))) break;
       tc_fence_after();
       uint32_t sr[4][32];
