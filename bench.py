@@ -50,7 +50,8 @@ def visible_pairs(wl) -> int:
             if jhi <= jlo:
                 continue
             if wl.causal:
-                cnt += int(np.clip(np.minimum(i + 1, jhi) - jlo, 0, None).sum())
+                lo = np.maximum(jlo, i - wl.window + 1) if wl.window > 0 else jlo   # sliding window
+                cnt += int(np.clip(np.minimum(i + 1, jhi) - lo, 0, None).sum())
             else:
                 cnt += i.size * (jhi - jlo)
         total += cnt * wl.H
@@ -148,8 +149,9 @@ def oracle_sample(wl, budget_s, inputs=None):
     spec = A.Spec(B=wl.B, H=wl.H, N=wl.N, d=wl.d, causal=wl.causal,
                   seqlens_k=None if wl.seqlens is None else np.asarray(wl.seqlens),
                   block_mask=None if wl.block_mask is None else wl.block_mask.astype(bool),
-                  dropout_p=wl.dropout_p, seed=wl.dropout_seed, offset=wl.dropout_offset)
-    one = wl.with_(B=1, H=1, seqlens=None if wl.seqlens is None else wl.seqlens[:1])
+                  dropout_p=wl.dropout_p, seed=wl.dropout_seed, offset=wl.dropout_offset, H_kv=wl.H_kv,
+                  window=wl.window)
+    one = wl.with_(B=1, H=1, H_kv=None, seqlens=None if wl.seqlens is None else wl.seqlens[:1])
     inp = W.make_inputs(one) if inputs is None else inputs
     q, k, v, do = (inp[n][0, 0].float().numpy().astype(np.float64) for n in ("q", "k", "v", "do"))
     head_flops = 2.5 * 4 * wl.d * visible_pairs(one)
@@ -236,6 +238,7 @@ def main():
     host = W.make_inputs(wl)
     t = {k: v.to(dev) for k, v in host.items()}
     kw = dict(causal=wl.causal, dropout_p=wl.dropout_p, seed=wl.dropout_seed, offset=wl.dropout_offset,
+              window=wl.window,
               seqlens_k=None if wl.seqlens is None else torch.from_numpy(np.asarray(wl.seqlens, np.int32)).to(dev),
               block_mask=None if wl.block_mask is None else torch.from_numpy(wl.block_mask.astype(np.uint8)).to(dev))
     pairs = visible_pairs(wl)
@@ -287,7 +290,8 @@ def main():
     e2e = None
     if not args.no_e2e:
         hp = {k: v.pin_memory() for k, v in host.items()}
-        outs = {n: torch.empty_like(hp["q"]).pin_memory() for n in ("o", "dq", "dk", "dv")}
+        outs = {n: torch.empty_like(hp["k" if n in ("dk", "dv") else "q"]).pin_memory()
+                for n in ("o", "dq", "dk", "dv")}
         lse_h = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in hp.values())
         d2h = sum(v.numel() * v.element_size() for v in outs.values()) + lse_h.numel() * 4
@@ -335,7 +339,8 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "causal": wl.causal,
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "H_kv": wl.hkv, "N": wl.N, "d": wl.d,
+                   "causal": wl.causal, "window": wl.window,
                    "dropout_p": wl.dropout_p, "parallelism": "replicas" if ws > 1 else "single",
                    "l2": "inputs exceed L2 (%.0f MB per step)" % (sum(v.numel() * v.element_size()
                                                                       for v in host.values()) / 1e6)},
@@ -363,13 +368,26 @@ def _launches_per_step(wl):
     return fwd + bwd
 
 
+def _source_hash(which):
+    import hashlib
+    m = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_io_aware_tiled_gb300", "csrc")
+    for f in ("%s_tc.cu" % which, "common.cuh", "fa_internal.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
+
+
 def _recorded_traffic(workload, which):
-    """DRAM bytes per launch recorded from an ncu capture of the current kernel (profiles/traffic.json)."""
+    """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json), or None
+    when there is none for this workload or the kernel sources changed since the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    return d.get(workload, {}).get(which)
+    rec = json.load(open(p)).get(workload, {})
+    if which not in rec or rec.get("source_sha256", {}).get(which) != _source_hash(which):
+        return None
+    return rec[which]
 
 
 if __name__ == "__main__":
