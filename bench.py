@@ -142,6 +142,12 @@ def _max_over_ranks(x, ws, device):
     return float(t.item())
 
 
+def replica_value(ws, step_flops, ms_max):
+    """Whole-job TFLOP/s: every one of the ws ranks did step_flops per step; the
+    step time is the slowest rank's (max over ranks)."""
+    return ws * step_flops / (ms_max * 1e-3) / 1e12
+
+
 def oracle_sample(wl, budget_s, inputs=None):
     """Time the float64 oracle (as it stands) on whole heads of `wl` for ~budget_s."""
     from oracle import attention as A
@@ -316,7 +322,7 @@ def main():
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = _max_over_ranks(a.elapsed_time(b) / KE, ws, dev)
-        e2e = {"value": ws * step_flops_headline / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": replica_value(ws, step_flops_headline, e2e_ms), "unit": "TFLOP/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     peaks, peak_kind = _peaks()
@@ -334,7 +340,7 @@ def main():
         v, heads, dt = oracle_sample(wl, args.cpu_budget)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
                "sample": "%d whole (b=0,h=0) heads fwd+bwd in %.1f s, float64 numpy" % (heads, dt)}
-    value = ws * step_flops_headline / (ms_max * 1e-3) / 1e12
+    value = replica_value(ws, step_flops_headline, ms_max)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -345,7 +351,7 @@ def main():
                    "l2": "inputs exceed L2 (%.0f MB per step)" % (sum(v.numel() * v.element_size()
                                                                       for v in host.values()) / 1e6)},
         "pct_of_bf16_peak": 100.0 * value / float(peaks["bf16_tflops_sustained"]) / ws,
-        "value_executed_flops": ws * step_flops_exec / (ms_max * 1e-3) / 1e12,
+        "value_executed_flops": replica_value(ws, step_flops_exec, ms_max),
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "roofline": {"kernel": "attn_%s_tc" % dominant, "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,

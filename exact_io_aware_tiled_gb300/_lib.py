@@ -20,8 +20,8 @@ _LIB_PATH = Path(__file__).resolve().parent / "libfa_gb300.so"
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_WORKSPACE, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(7)
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
-EXPORTED = ["fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd", "fa_check_status",
-            "fa_dropout_mask", "fa_status_string", "fa_version"]
+EXPORTED = ["fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd", "fa_bwd_noalloc",
+            "fa_check_status", "fa_dropout_mask", "fa_selftest_wait_timeout", "fa_status_string", "fa_version"]
 
 
 class fa_params(ctypes.Structure):
@@ -234,6 +234,22 @@ def dropout_mask(B, H, N, b, h, row0, nrows, *, dropout_p, seed=0, offset=0, dev
     if st != FA_OK:
         raise FAError(st, "fa_dropout_mask")
     return out
+
+
+def selftest_wait_timeout(device="cuda", stream=None):
+    """Run fa_selftest_wait_timeout: returns (status, gave_up[2], waited_ns of the second warp)."""
+    lib = load()
+    fn = lib.fa_selftest_wait_timeout
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    ws = torch.empty(256, device=device, dtype=torch.uint8)
+    out = torch.zeros(2, device=device, dtype=torch.int32)
+    ns = torch.zeros(1, device=device, dtype=torch.int64)
+    st = fn(_ptr(ws), _ptr(out), _ptr(ns), _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_selftest_wait_timeout")
+    status = check_status(ws, stream)
+    return status, out.cpu().tolist(), int(ns.item())
 
 
 def default_scale(d: int) -> float:

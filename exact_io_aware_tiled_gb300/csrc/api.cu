@@ -329,6 +329,17 @@ fa_status fa_dropout_mask(const fa_params* p, int32_t b, int32_t h, int32_t row0
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fa_status fa_selftest_wait_timeout(void* ws, int32_t* out, uint64_t* out_ns, void* stream) {
+  if (ws == nullptr || out == nullptr || out_ns == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(out_ns) & 7u) != 0) return FA_ERR_MISALIGNED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), st);
+  if (e == cudaSuccess)
+    e = launch_wait_selftest(static_cast<int*>(ws), reinterpret_cast<int*>(out),
+                             reinterpret_cast<unsigned long long*>(out_ns), st);
+  return cuda_status(e);
+}
+
 const char* fa_status_string(fa_status s) {
   switch (s) {
     case FA_OK: return "FA_OK";

@@ -7,7 +7,9 @@
 //   * dq_convert: float32 dQ accumulator -> storage dtype;
 //   * block_lists: row / column index lists of a block-sparse mask
 //     (agihunt.info, block-sparse paragraph: only nonzero blocks are visited);
-//   * dropout_mask: the keep-mask of the Philox mapping, for tests.
+//   * dropout_mask: the keep-mask of the Philox mapping, for tests;
+//   * wait_selftest: the bounded-wait path of the attention kernels, run on
+//     mbarriers that nothing ever arrives at.
 #include "common.cuh"
 
 namespace fa {
@@ -186,6 +188,42 @@ cudaError_t launch_dropout_mask(const DropoutArgs& d, int H, int N, int b, int h
   const int threads = 256;
   dropout_mask_kernel<<<(unsigned)((groups + threads - 1) / threads), threads, 0, s>>>(d, H, N, b, h, row0, nrows,
                                                                                          out);
+  return cudaGetLastError();
+}
+
+// Two warps each wait, with the same bounded wait the attention kernels
+// use, on an mbarrier that nothing arrives at.  Warp 1 starts its wait half
+// the limit later than warp 0.  Warp 0's wait runs out first, records
+// FA_ERR_TIMEOUT in the status word and raises the CTA abort flag; warp 1's
+// wait then returns on the flag, about half the limit after it started,
+// instead of running its own limit out.  out[w] = 1 if warp w's wait
+// returned false; out_ns = how long warp 1's wait lasted.
+__global__ void wait_selftest_kernel(int* status, int* out, unsigned long long* out_ns) {
+  __shared__ uint64_t bars[2];
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  WaitCtl ctl{status, &abort_flag};
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    if (w == 1) {   // a bounded delay of half the wait limit
+      const uint64_t d0 = globaltimer_ns();
+      while (globaltimer_ns() - d0 < kWaitTimeoutNs / 2) __nanosleep(1000);
+    }
+    const uint64_t t0 = globaltimer_ns();
+    const bool ok = mbar_wait(&bars[w], 0, ctl);
+    out[w] = ok ? 0 : 1;
+    if (w == 1) *out_ns = globaltimer_ns() - t0;
+  }
+}
+
+cudaError_t launch_wait_selftest(int* status, int* out, unsigned long long* out_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 64, 0, s>>>(status, out, out_ns);
   return cudaGetLastError();
 }
 

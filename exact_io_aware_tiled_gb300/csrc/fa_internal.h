@@ -92,5 +92,6 @@ cudaError_t launch_block_lists(const uint8_t* mask, int nb, int16_t* row_list, i
                                int16_t* col_list, int32_t* col_cnt, cudaStream_t s);
 cudaError_t launch_dropout_mask(const DropoutArgs& d, int H, int N, int b, int h, int row0, int nrows,
                                 uint8_t* out, cudaStream_t s);
+cudaError_t launch_wait_selftest(int* status, int* out, unsigned long long* out_ns, cudaStream_t s);
 
 }  // namespace fa

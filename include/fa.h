@@ -198,6 +198,25 @@ fa_status fa_check_status(const void *ws, void *stream);
 fa_status fa_dropout_mask(const fa_params *p, int32_t b, int32_t h, int32_t row0,
                           int32_t nrows, uint8_t *out, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * fa_selftest_wait_timeout -- exercises the bounded device-side wait that
+ * every attention kernel uses, without any attention work and without a
+ * fault: one CTA of two warps waits on mbarriers that nothing arrives at,
+ * the second warp starting one second after the first.  The first wait
+ * gives up after the library's limit (2 s of %globaltimer), records
+ * FA_ERR_TIMEOUT in the status word at the start of `ws` and raises the
+ * CTA's abort flag; the second wait then returns on that flag, about one
+ * second after it began.  The kernel exits normally and the context stays
+ * usable.
+ *   ws    : device workspace of >= 256 bytes (the status word is cleared
+ *           first, as fa_fwd / fa_bwd do)
+ *   out   : device int32[2]: 1 where a warp's wait returned "gave up"
+ *   out_ns: device uint64[1]: nanoseconds the second warp waited
+ * fa_check_status(ws) then returns FA_ERR_TIMEOUT.  For tests of the
+ * failure path; it takes about two seconds.
+ * ------------------------------------------------------------------------- */
+fa_status fa_selftest_wait_timeout(void *ws, int32_t *out, uint64_t *out_ns, void *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *fa_status_string(fa_status s);
 
