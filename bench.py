@@ -378,7 +378,7 @@ def _source_hash(which):
     import hashlib
     m = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_io_aware_tiled_gb300", "csrc")
-    for f in ("%s_tc.cu" % which, "common.cuh", "fa_internal.h"):
+    for f in ("%s_tc.cu" % which, "common.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             m.update(fh.read())
     return m.hexdigest()[:16]
