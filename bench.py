@@ -292,38 +292,63 @@ def main():
     bwd_ms = sum(a.elapsed_time(b) for a, b in evb) / K
     ms_max = _max_over_ranks(ms, ws, dev)
 
-    # end to end: pinned host inputs -> device, fwd + bwd, gradients and O back to pinned host
+    # end to end: pinned host inputs -> device, fwd + bwd, O, LSE and the
+    # gradients back to pinned host memory, every step.  Consecutive steps
+    # are pipelined the way a caller streaming batches would run them: the
+    # host-to-device copy of step i+1 and the device-to-host copy of step
+    # i-1 run on their own streams while step i computes (two device input
+    # sets, two host output sets).
     e2e = None
     if not args.no_e2e:
         hp = {k: v.pin_memory() for k, v in host.items()}
-        outs = {n: torch.empty_like(hp["k" if n in ("dk", "dv") else "q"]).pin_memory()
-                for n in ("o", "dq", "dk", "dv")}
-        lse_h = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32).pin_memory()
+        kv_like = lambda n: "k" if n in ("dk", "dv") else "q"
+        hout = [{n: torch.empty_like(hp[kv_like(n)]).pin_memory() for n in ("o", "dq", "dk", "dv")}
+                for _ in range(2)]
+        for ho in hout:
+            ho["lse"] = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32).pin_memory()
+        dsets = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
         h2d = sum(v.numel() * v.element_size() for v in hp.values())
-        d2h = sum(v.numel() * v.element_size() for v in outs.values()) + lse_h.numel() * 4
+        d2h = sum(v.numel() * v.element_size() for v in hout[0].values())
+        s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_cmp = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step():
-            d = {k: v.to(dev, non_blocking=True) for k, v in hp.items()}
-            o, lse = fa.fwd(d["q"], d["k"], d["v"], **kw)
-            dq, dk, dv = fa.bwd(d["q"], d["k"], d["v"], o, d["do"], lse, **kw)
-            for n, x in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
-                outs[n].copy_(x, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
+        def e2e_step(i):
+            x = i % 2
+            d = dsets[x]
+            s_in.wait_event(ev_cmp[x])          # step i-2 has finished reading this input set
+            with torch.cuda.stream(s_in):
+                for k in d:
+                    d[k].copy_(hp[k], non_blocking=True)
+                ev_in[x].record(s_in)
+            s_cmp.wait_event(ev_in[x])
+            with torch.cuda.stream(s_cmp):
+                o, lse = fa.fwd(d["q"], d["k"], d["v"], **kw)
+                dq, dk, dv = fa.bwd(d["q"], d["k"], d["v"], o, d["do"], lse, **kw)
+                ev_cmp[x].record(s_cmp)
+            s_out.wait_event(ev_cmp[x])
+            with torch.cuda.stream(s_out):
+                for n, t_ in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+                    hout[x][n].copy_(t_, non_blocking=True)
+                    t_.record_stream(s_out)
 
-        for _ in range(2):
-            e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize()
         _barrier(ws)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        KE = max(3, K // 2)
-        a.record(stream)
-        for _ in range(KE):
-            e2e_step()
-        b.record(stream)
+        KE = max(4, K // 2)
+        a.record(s_in)
+        for i in range(KE):
+            e2e_step(i)
+        s_out.wait_stream(s_in)
+        s_out.wait_stream(s_cmp)
+        b.record(s_out)
         torch.cuda.synchronize()
         e2e_ms = _max_over_ranks(a.elapsed_time(b) / KE, ws, dev)
         e2e = {"value": replica_value(ws, step_flops_headline, e2e_ms), "unit": "TFLOP/s",
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "pipelined": "H2D of step i+1 and D2H of step i-1 overlap step i's kernels"}
 
     peaks, peak_kind = _peaks()
     dominant = "bwd" if bwd_ms >= fwd_ms else "fwd"
