@@ -412,7 +412,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       }
       l_true += (lt[0] + lt[1]) + (lt[2] + lt[3]);
       l_rnd += ((lr[0] + lr[1]) + (lr[2] + lr[3])) / pscale;
-      if (rescale) {
+      // tcgen05.ld / st are warp-collective: the warp rescales together when
+      // any of its rows needs it (alpha is exactly 1 for the other rows)
+      if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t o[32];

@@ -102,7 +102,7 @@ def make_inputs(wl: Workload, grads: bool = True):
     return out
 
 
-# The five workloads (name -> Workload).  Seeds are 20260 + index.
+# The workloads (name -> Workload).  Seeds are 20260 + index.
 CONFIGS = {
     "tiny_f32": Workload("tiny_f32", B=1, H=2, N=256, dtype="f32", seed=20261),
     "gpt2_medium_causal": Workload("gpt2_medium_causal", B=64, H=16, N=1024,
@@ -115,4 +115,12 @@ CONFIGS = {
                                        seed=20264),
     "butterfly_sparse_64k": Workload("butterfly_sparse_64k", B=1, H=8, N=65536,
                                      dtype="bf16", sparse_butterfly=True, seed=20265),
+    # grouped-query attention at the GPT-2-medium shape with 8 K/V heads
+    # (living-dl-book, section 6: GQA-8)
+    "gqa8_gpt2_medium_causal": Workload("gqa8_gpt2_medium_causal", B=64, H=16, N=1024, H_kv=8,
+                                        dtype="bf16", causal=True, seed=20266),
+    # the sliding-window exercise of lynx-cortex ("Problemas de práctica"):
+    # N = 8192 with a window of 512 keys
+    "window512_8k": Workload("window512_8k", B=4, H=16, N=8192, dtype="bf16", causal=True,
+                             window=512, seed=20267),
 }

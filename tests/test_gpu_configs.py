@@ -66,3 +66,23 @@ def test_butterfly_sparse_64k():
     rows = sample_rows(wl.N, seed=6, extra=128)
     cols = np.concatenate([np.arange(0, 40), np.arange(128 * 255 - 3, 128 * 255 + 40), np.arange(wl.N - 40, wl.N)])
     check_head(wl, inp, got, 0, 5, rows=rows, cols=cols)
+
+
+def test_gqa8_gpt2_medium_causal():
+    wl = W.CONFIGS["gqa8_gpt2_medium_causal"]
+    inp = W.make_inputs(wl)
+    got = run_gpu(wl, inp)
+    for b, h in [(0, 1), (63, 15), (40, 9)]:       # odd heads: each closes a K/V group (dK, dV checked)
+        check_head(wl, inp, got, b, h)
+    rows = sample_rows(wl.N, seed=66, extra=64)
+    check_head(wl, inp, got, 21, 7, rows=rows, cols=rows)
+
+
+def test_window512_8k():
+    wl = W.CONFIGS["window512_8k"]
+    inp = W.make_inputs(wl)
+    got = run_gpu(wl, inp)
+    rows = sample_rows(wl.N, seed=77, extra=128)
+    cols = np.unique(np.concatenate([np.arange(0, 64), np.arange(4000, 4200), np.arange(wl.N - 128, wl.N)]))
+    check_head(wl, inp, got, 3, 12, rows=rows, cols=cols)
+    check_head(wl, inp, got, 0, 0, rows=rows[:200], cols=cols[:100])

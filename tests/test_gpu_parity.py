@@ -145,3 +145,21 @@ def test_sliding_window_requires_causal():
     q = torch.zeros((1, 1, 128, 64), device="cuda", dtype=torch.bfloat16)
     with pytest.raises(fa.FAError):
         fa.fwd(q, q, q, window=16)
+
+
+def test_rescale_decided_per_row_within_a_warp():
+    # Rows alternate between a large and a small query norm, and the second key
+    # tile is much larger than the first.  At the second tile the running max
+    # of the large-norm rows jumps past the rescale threshold while that of the
+    # small-norm rows does not, so neighbouring rows of one warp disagree on
+    # whether O must be rescaled.
+    wl = _wl(256, "bf16", B=1, H=2, seed=13)
+    inp = W.make_inputs(wl)
+    qs = torch.where(torch.arange(256) % 2 == 0, 4.0, 0.1).view(1, 1, 256, 1)
+    ks = torch.where(torch.arange(256) < 128, 0.1, 4.0).view(1, 1, 256, 1)
+    inp["q"] = (inp["q"].float() * qs).to(torch.bfloat16)
+    inp["k"] = (inp["k"].float() * ks).to(torch.bfloat16)
+    for w in (wl, wl.with_(causal=True)):
+        got = run_gpu(w, inp)
+        for h in range(w.H):
+            check_head(w, inp, got, 0, h)
