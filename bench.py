@@ -332,12 +332,12 @@ def main():
                     hout[x][n].copy_(t_, non_blocking=True)
                     t_.record_stream(s_out)
 
-        for i in range(2):
+        for i in range(4):                      # both buffer sets, twice
             e2e_step(i)
         torch.cuda.synchronize()
         _barrier(ws)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        KE = max(4, K // 2)
+        KE = max(6, K // 2)
         a.record(s_in)
         for i in range(KE):
             e2e_step(i)
