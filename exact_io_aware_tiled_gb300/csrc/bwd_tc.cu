@@ -389,12 +389,24 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       tmem_ld16(tl + kColST + c0, sv[0]);
       uint32_t keep = ~0u;
       if constexpr (kDrop) {
+        // One Philox call covers 8 consecutive keys of one query row, and the
+        // 8 lanes 8m..8m+7 hold 8 consecutive keys (j & 7 == lane & 7).  So
+        // lane t of each group evaluates the calls of queries t, t+8, t+16,
+        // t+24 (4 instead of 32), packs their 8-key keep bytes into one word,
+        // and the group exchanges the words.
+        const int t8 = lane & 7;
+        uint32_t mine = 0;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t q = (uint32_t)(qi * kTile + c0 + t8 + 8 * m);
+          mine |= dropout_keep8((uint32_t)j >> 3, bh_rows + q, a.drop) << (8 * m);
+        }
         uint32_t kb = 0;
-#pragma unroll 4
-        for (int c = 0; c < 32; ++c) {
-          const uint32_t q = (uint32_t)(qi * kTile + c0 + c);
-          const uint32_t bits = dropout_keep8((uint32_t)j >> 3, bh_rows + q, a.drop);
-          kb |= ((bits >> (j & 7)) & 1u) << c;
+#pragma unroll
+        for (int src = 0; src < 8; ++src) {
+          const uint32_t w = __shfl_sync(0xffffffffu, mine, (lane & ~7) | src);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) kb |= ((w >> (8 * m + t8)) & 1u) << (src + 8 * m);
         }
         keep = kb;
       }
