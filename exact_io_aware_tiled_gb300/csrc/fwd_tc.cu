@@ -111,6 +111,12 @@ struct StepPlan {
   uint32_t ph[2];         // phase parity of each load
   int kv[2];              // kv tile of each load
   int use[2];             // load index used by slot x, or -1
+  // Accessors by select rather than by indexing with a run-time value, so
+  // the plan stays in registers (an indexed array would live in local memory
+  // and cost the single-thread issuers a memory round trip per access).
+  __device__ __forceinline__ int stage(int l) const { return l ? st[1] : st[0]; }
+  __device__ __forceinline__ uint32_t parity(int l) const { return l ? ph[1] : ph[0]; }
+  __device__ __forceinline__ int load_of(int x) const { return x ? use[1] : use[0]; }
 };
 
 template <bool kWin>
@@ -210,6 +216,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const uint32_t qbytes = (sl[0].n > 0 ? 16384u : 0u) + (sl[1].n > 0 ? 16384u : 0u);
       if (qbytes > 0) {
         mbar_expect_tx(&bars->q_full, qbytes);
+#pragma unroll
         for (int x = 0; x < 2; ++x)
           if (sl[x].n > 0) tma_load_4d(smem + C::kQ + x * 16384, &tmQ, &bars->q_full, 0, sl[x].qt * kTile, h, b);
       }
@@ -217,7 +224,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       bool ok = true;
       for (int s = 0; s < smax && ok; ++s) {
         const StepPlan p = plan_step<kWin>(sl, s, ld);
-        for (int l = 0; l < p.nl; ++l) {
+#pragma unroll
+        for (int l = 0; l < 2; ++l) {
+          if (l >= p.nl) break;
           const int st = p.st[l];
           if (!(ok = mbar_wait(&bars->k_empty[st], p.ph[l] ^ 1u, ctl) &&
                      mbar_wait(&bars->v_empty[st], p.ph[l] ^ 1u, ctl)))
@@ -246,19 +255,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       int ld = 0;
       for (int s = 0; s < smax && ok; ++s) {
         const StepPlan p = plan_step<kWin>(sl, s, ld);
-        for (int x = 0; x < 2 && ok; ++x) {
-          if (s >= sl[x].n) continue;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (!ok || s >= sl[x].n) continue;
           const int l = p.use[x];
           if (s > 0 && !(ok = mbar_wait(&bars->s_free[x], (uint32_t)(s - 1) & 1u, ctl))) break;
-          if (!(ok = mbar_wait(&bars->k_full[p.st[l]], p.ph[l], ctl))) break;
+          if (!(ok = mbar_wait(&bars->k_full[p.stage(l)], p.parity(l), ctl))) break;
           tc_fence_after();
-          const uint64_t kd = kd0 + (uint64_t)((p.st[l] * 16384) >> 4);
+          const uint64_t kd = kd0 + (uint64_t)((p.stage(l) * 16384) >> 4);
           const uint32_t tS = tmem + x * 256;
 #pragma unroll
           for (int k = 0; k < 4; ++k) mma_ss(tS, qd[x] + 2 * k, kd + 2 * k, idS, k > 0 ? 1u : 0u);
           mma_commit(&bars->s_full[x]);
         }
-        for (int l = 0; l < p.nl && ok; ++l) mma_commit(&bars->k_empty[p.st[l]]);
+#pragma unroll
+        for (int l = 0; l < 2; ++l)
+          if (ok && l < p.nl) mma_commit(&bars->k_empty[p.st[l]]);
       }
       mma_commit(&bars->done[0]);
       mbar_wait(&bars->done[0], 0, ctl);
@@ -270,16 +282,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       constexpr uint32_t idPV = idesc_f16(128, 64, ab, 0, 1);
       const uint64_t vd0 = sdesc_sw128(smem_u32(smem + C::kV), 16384, 1024);
       const uint32_t tP = tmem + x * 256 + 128, tO = tmem + x * 256 + 192;
-      const int n = sl[x].n;
+      const int n = x ? sl[1].n : sl[0].n;
       int ld = 0;
       bool ok = true;
       for (int s = 0; s < smax && ok; ++s) {
         const StepPlan p = plan_step<kWin>(sl, s, ld);
+        const int mine = p.load_of(x);
         if (s < n) {
-          const int l = p.use[x];
-          const int st = p.st[l];
+          const int st = p.stage(mine);
           if (!(ok = mbar_wait(&bars->p_full[x], (uint32_t)s & 1u, ctl) &&
-                     mbar_wait(&bars->v_full[st], p.ph[l], ctl)))
+                     mbar_wait(&bars->v_full[st], p.parity(mine), ctl)))
             break;
           tc_fence_after();
           const uint64_t vd = vd0 + (uint64_t)((st * 16384) >> 4);
@@ -290,11 +302,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         // one arrival per slot on every loaded stage: after our MMAs for a
         // stage we read, right away (once it is loaded) for one we did not
-        for (int l = 0; l < p.nl && ok; ++l) {
-          if (s < n && l == p.use[x]) {
+#pragma unroll
+        for (int l = 0; l < 2; ++l) {
+          if (!ok || l >= p.nl) continue;
+          if (s < n && l == mine) {
             mma_commit(&bars->v_empty[p.st[l]]);
           } else {
-            if (!(ok = mbar_wait(&bars->v_full[p.st[l]], p.ph[l], ctl))) break;
+            if (!(ok = mbar_wait(&bars->v_full[p.st[l]], p.ph[l], ctl))) continue;
             mbar_arrive(&bars->v_empty[p.st[l]]);
           }
         }
