@@ -40,10 +40,13 @@ template <typename T> struct Vec8 {
   }
 };
 
+// It also clears the float32 dQ accumulator row (when there is one): the
+// same threads write the row's 64 zeros, 32 bytes each, so the clearing
+// rides on this pass instead of a separate memset.
 template <typename T>
 __global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ dout, Strides st,
                                 const float* __restrict__ lse, int B, int H, int N, int npad,
-                                float* __restrict__ lse2, float* __restrict__ dvec) {
+                                float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dqacc) {
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 3;
   const int part = threadIdx.x & 7;
   const long long total = (long long)B * H * npad;
@@ -55,6 +58,11 @@ __global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ d
     const int b = bh / H, h = bh % H;
     const size_t off = (size_t)b * st.b + (size_t)h * st.h + (size_t)i * st.n + part * 8;
     d = Vec8<T>::dot(o + off, dout + off);
+    if (dqacc != nullptr) {
+      float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * N + i) * 64 + part * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   d += __shfl_xor_sync(0xffffffffu, d, 1);
   d += __shfl_xor_sync(0xffffffffu, d, 2);
@@ -147,17 +155,14 @@ cudaError_t launch_bwd_prep(int dtype, const void* o, const void* dout, Strides 
   const long long blocks = (rows * 8 + threads - 1) / threads;
   if (dtype == FA_DT_BF16)
     bwd_prep_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, s>>>(
-        (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, st, lse, B, H, N, npad, lse2, dvec);
+        (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, st, lse, B, H, N, npad, lse2, dvec, dqacc);
   else if (dtype == FA_DT_F16)
     bwd_prep_kernel<__half><<<(unsigned)blocks, threads, 0, s>>>((const __half*)o, (const __half*)dout, st, lse, B,
-                                                                 H, N, npad, lse2, dvec);
+                                                                 H, N, npad, lse2, dvec, dqacc);
   else
     bwd_prep_kernel<float><<<(unsigned)blocks, threads, 0, s>>>((const float*)o, (const float*)dout, st, lse, B, H,
-                                                                N, npad, lse2, dvec);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (dqacc != nullptr) e = cudaMemsetAsync(dqacc, 0, (size_t)B * H * N * 64 * sizeof(float), s);
-  return e;
+                                                                N, npad, lse2, dvec, dqacc);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_dq_convert(int dtype, const float* dqacc, void* dq, Strides st, int B, int H, int N,

@@ -80,7 +80,7 @@ cudaError_t launch_bwd_simt(const float* q, const float* k, const float* v, cons
                             float* dq, float* dk, float* dv, Strides st, Strides kst, const BwdArgs& a,
                             cudaStream_t s);
 
-// D = rowsum(dO o O) and the padded LSE*log2e / D arrays; zeroes dqacc if given.
+// D = rowsum(dO o O) and the padded LSE*log2e / D arrays; the same pass clears dqacc if given.
 cudaError_t launch_bwd_prep(int dtype, const void* o, const void* dout, Strides st, const float* lse,
                             int B, int H, int N, int npad, float* lse2, float* dvec, float* dqacc,
                             cudaStream_t s);
