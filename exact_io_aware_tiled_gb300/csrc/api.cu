@@ -294,16 +294,18 @@ fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v
     return cuda_status(launch_bwd_simt((const float*)q, (const float*)k, (const float*)v, (const float*)dout,
                                        (float*)dq, (float*)dk, (float*)dv, sd, skv, a, st));
   }
-  CUtensorMap mq, mk, mv, mdo, mdk, mdv, macc;
+  CUtensorMap mq, mk, mv, mdo, macc;
   Strides acc_st{(int64_t)p->H * p->N * kHeadDim, (int64_t)p->N * kHeadDim, kHeadDim};
   if ((s = map16(&mq, q, p, p->H, sd)) != FA_OK || (s = map16(&mk, k, p, hkv, skv)) != FA_OK ||
       (s = map16(&mv, v, p, hkv, skv)) != FA_OK || (s = map16(&mdo, dout, p, p->H, sd)) != FA_OK ||
-      (s = map16(&mdk, dk, p, hkv, skv)) != FA_OK || (s = map16(&mdv, dv, p, hkv, skv)) != FA_OK ||
       (s = make_map(&macc, dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kHeadDim, 32, p, p->H, acc_st)) != FA_OK)
     return s;
+  a.dk = dk;
+  a.dv = dv;
+  a.kst = skv;
   {
     ProfScope prof(p, st);
-    if ((e = launch_bwd_tc(p->dtype, mq, mk, mv, mdo, mdk, mdv, macc, a, st)) != cudaSuccess) return FA_ERR_CUDA;
+    if ((e = launch_bwd_tc(p->dtype, mq, mk, mv, mdo, macc, a, st)) != cudaSuccess) return FA_ERR_CUDA;
   }
   return cuda_status(launch_dq_convert(p->dtype, dqacc, dq, sd, p->B, p->H, p->N, st));
 }

@@ -10,26 +10,32 @@
 //     dP^T = Z o (V dO_i^T) / (1 - p)
 //     dS^T = P^T o (dP^T - D_i)
 //     dV += P~^T dO_i,  dK += dS^T Q_i,  dQ_i += dS K      (tau applied at the end)
-//
 // Grouped-query attention (living-dl-book, "Atencao eficiente", section 6):
 // dK and dV of a K/V head shared by g query heads sum over those heads.  The
 // sliding window (lynx-cortex, "Problemas de practica") limits the query
 // tiles that see a key tile and masks the window's far edge.
 //
-// GB300 mapping (ours): one CTA per (b, K/V head, 128-key tile), looping over
-// the query tiles that see it for each query head of the group, so dK and dV
-// accumulate over the group in tensor memory; the CTAs of one head are
-// adjacent in launch order so its Q / dO tiles and dQ accumulator rows stay
-// in L2.
-//   * warp 16: TMA loads of K, V once and of Q_i, dO_i (+ LSE_i, D_i rows)
-//     into a three-stage ring, and the two TMA reduce-adds of each staged
-//     dQ_i into the float32 accumulator;
+// GB300 mapping (ours): a persistent kernel, one CTA per SM.  The work items
+// are (b, K/V head, 128-key tile); CTA c takes, from each block of G
+// consecutive items (G = the grid), item (c + k) mod G of block k, so that
+// every CTA sees every key-tile position (the causal work per item varies
+// with it) while the CTAs working at one time cover a few adjacent heads,
+// whose Q / dO tiles and dQ accumulator rows stay in L2.  Per item the CTA
+// loops over the query tiles that see the key tile, for each query head of
+// the group, so dK and dV accumulate over the group in tensor memory.  The
+// steps of consecutive items form one global sequence: every ring and
+// barrier phase runs on the global step index, K/V are double-buffered so
+// the next item's K/V load overlaps the current item, and an item's dK, dV
+// leave tensor memory while the next item starts.
+//   * warp 16: TMA loads of K, V per item and of Q_i, dO_i (+ LSE_i, D_i
+//     rows) per step into a two-stage ring, and, three steps behind, the two
+//     TMA reduce-adds of each staged dQ_i into the float32 accumulator;
 //   * three MMA-issuing warps (one thread each): consecutive MMAs into the
 //     same accumulator complete about 126 cycles apart whatever their N, so
 //     each product is a latency chain, and independent chains are issued
 //     from separate warps so that they overlap:
-//       warp 17: S^T(i+1) = K Q_{i+1}^T and dP^T(i+1) = V dO_{i+1}^T, each
-//                as soon as the softmax warps have read the previous one;
+//       warp 17: S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T, each as soon as
+//                the softmax warps have read the previous one;
 //       warp 18: dV += P~^T dO_i (A from tensor memory) and
 //                dK += dS^T Q_i (A from the shared dS^T tile);
 //       warp 19: dQ_i = dS K (A = the same tile read MN-major);
@@ -39,11 +45,15 @@
 //       part 2: dS from dP^T, dS^T (16 bit) into a swizzled shared tile
 //               that both dK and dQ read;
 //       drain:  16 of the 64 columns of dQ_i from tensor memory -> x tau ->
-//               shared staging.
+//               shared staging (in the following step);
+//       item end: 16 of the 64 columns of dK (x tau) and dV from tensor
+//               memory straight to global memory.
 // Tensor memory (512 columns):
 //   S^T 0-127 | dP^T 128-255 | dK 256-319 | dV 320-383 | dQ 384-447 |
 //   P~^T (16 bit, queries 32w..32w+31 packed at 448+16w .. +16) 448-511.
 // Registers: 96 a thread (640 threads, one CTA per SM).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace fa {
@@ -51,24 +61,26 @@ namespace {
 
 constexpr int kThreads = 640;
 constexpr int kCompute = 512;   // threads of warps 0-15
-constexpr int NSB = 3;   // Q / dO stages
+constexpr int NSB = 2;   // Q / dO stages
 constexpr int NSTG = 1;  // float32 dQ staging buffers
+constexpr int kLag = 3;  // dQ reduce-adds trail the loads by this many steps
 
 struct BwdSmem {
-  static constexpr int kK = 0;
-  static constexpr int kV = 16384;
-  static constexpr int kQ = 32768;                  // NSB x 16 KB
+  static constexpr int kK = 0;                      // 2 x 16 KB (double-buffered per item)
+  static constexpr int kV = 32768;                  // 2 x 16 KB
+  static constexpr int kQ = 65536;                  // NSB x 16 KB
   static constexpr int kDO = kQ + NSB * 16384;      // NSB x 16 KB
   static constexpr int kDS = kDO + NSB * 16384;     // 32 KB: dS^T [2 chunks][128 keys][64 q]
   static constexpr int kDQ = kDS + 32768;           // NSTG x 32 KB: float32 dQ staging [buf][half][128][32]
   static constexpr int kLD = kDQ + NSTG * 32768;    // NSB x (LSE2[128] + D[128]) floats
-  static constexpr int kBar = kLD + NSB * 1024;
+  static constexpr int kInfo = kLD + NSB * 1024;    // (query tile, query head, batch) of the last kLag+1 steps
+  static constexpr int kBar = kInfo + 64;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kDyn = kBytes + 1024;
 };
 
 struct BBars {
-  uint64_t kv_full;
+  uint64_t kv_full[2], kv_empty[2];
   uint64_t q_full[NSB], q_empty[NSB];
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free, dkv_full, pt_free;
   uint64_t dsm_free;
@@ -79,15 +91,71 @@ struct BBars {
 };
 
 static_assert(sizeof(BBars) <= 256, "barrier block overflows its shared-memory slot");
+static_assert(BwdSmem::kDyn <= 232448, "shared memory over the per-block limit");
 
-// The steps of one CTA: every query tile that sees its key tile, for each of
-// the g query heads that share its K/V head (head-major: step t is tile
-// t % n of query head h0 + t / n; the loops track both with counters).
-struct QList {
+// One work item: key tile jt of K/V head hk of batch b, and its steps:
+// every query tile that sees the key tile, for each of the g query heads
+// that share the K/V head (head-major: step t is tile t % n of query head
+// h0 + t / n; the loops track both with counters).
+struct Item {
+  int b, hk, jt, Lk;
   int n;                  // query tiles per query head
   int i0;                 // first query tile (dense)
   int h0;                 // first query head of the group
   const int16_t* list;    // sparse list or nullptr
+  int steps;              // n * g
+  __device__ __forceinline__ int qt(int u) const { return list ? (int)list[u] : i0 + u; }
+};
+
+__device__ __forceinline__ Item make_item(const BwdArgs& a, int u) {
+  Item it;
+  const int bk = u / a.nq;
+  it.jt = u - bk * a.nq;
+  it.b = bk / a.H_kv;
+  it.hk = bk - it.b * a.H_kv;
+  it.Lk = a.N;
+  if (a.mask.seqlens_k != nullptr) it.Lk = max(0, min(a.N, a.mask.seqlens_k[it.b]));
+  it.list = nullptr;
+  it.i0 = a.mask.causal ? it.jt : 0;
+  it.h0 = it.hk * a.group;
+  it.n = 0;
+  // last query tile that sees this key tile: under a sliding window of w keys,
+  // key j is seen by queries j .. j + w - 1
+  int qlast = a.nq - 1;
+  if (a.mask.window > 0) qlast = min(qlast, (it.jt * kTile + kTile - 1 + a.mask.window - 1) / kTile);
+  if (it.jt * kTile < it.Lk) {
+    if (a.mask.col_list != nullptr) {
+      const int16_t* list = a.mask.col_list + (size_t)it.jt * a.mask.nb;
+      const int cnt = a.mask.col_cnt[it.jt];
+      int s0 = 0;
+      if (a.mask.causal) while (s0 < cnt && list[s0] < it.jt) ++s0;
+      int e = s0;
+      while (e < cnt && list[e] <= qlast) ++e;
+      it.list = list + s0;
+      it.n = e - s0;
+    } else {
+      it.n = max(0, qlast - it.i0 + 1);
+    }
+  }
+  it.steps = it.n * a.group;
+  return it;
+}
+
+// The items of CTA c, in order: item (c + k) mod G of block k (items
+// k*G .. k*G + G - 1), skipping those past the end.
+struct ItemSeq {
+  int c, G, total, k;
+  __device__ __forceinline__ bool next(int& u) {
+    while (k * G < total) {
+      const int v = k * G + (c + k) % G;
+      ++k;
+      if (v < total) {
+        u = v;
+        return true;
+      }
+    }
+    return false;
+  }
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
@@ -101,7 +169,6 @@ template <typename T, bool kDrop, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-              const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
               const __grid_constant__ CUtensorMap tmDQ, const BwdArgs a) {
   using L = BwdSmem;
   extern __shared__ uint8_t smem_raw[];
@@ -109,42 +176,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   BBars* bars = reinterpret_cast<BBars*>(smem + L::kBar);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work item: (b, h, key tile jt); the tiles of one head are adjacent,
-  //      and under causal masking the longest query lists come first.
-  const int bk = (int)(blockIdx.x / a.nq);
-  const int jt = (int)(blockIdx.x % a.nq);
-  const int b = bk / a.H_kv, hk = bk % a.H_kv;   // K/V head
-  int Lk = a.N;
-  if (a.mask.seqlens_k != nullptr) Lk = max(0, min(a.N, a.mask.seqlens_k[b]));
-  QList ql;
-  ql.list = nullptr;
-  ql.i0 = a.mask.causal ? jt : 0;
-  ql.h0 = hk * a.group;
-  ql.n = 0;
-  // last query tile that sees this key tile: under a sliding window of w keys,
-  // key j is seen by queries j .. j + w - 1
-  int qlast = a.nq - 1;
-  if (a.mask.window > 0) qlast = min(qlast, (jt * kTile + kTile - 1 + a.mask.window - 1) / kTile);
-  if (jt * kTile < Lk) {
-    if (a.mask.col_list != nullptr) {
-      const int16_t* list = a.mask.col_list + (size_t)jt * a.mask.nb;
-      const int cnt = a.mask.col_cnt[jt];
-      int s0 = 0;
-      if (a.mask.causal) while (s0 < cnt && list[s0] < jt) ++s0;
-      int e = s0;
-      while (e < cnt && list[e] <= qlast) ++e;
-      ql.list = list + s0;
-      ql.n = e - s0;
-    } else {
-      ql.n = max(0, qlast - ql.i0 + 1);
-    }
-  }
-  const int n = ql.n * a.group;   // steps
+  const int total = a.nq * a.B * a.H_kv;
   WaitCtl ctl{a.status, &bars->abort};
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 2);   // S/dP warp and dQ warp read K / V
+    }
     for (int s = 0; s < NSB; ++s) {
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1);
@@ -180,143 +219,170 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     constexpr uint32_t idST = idesc_f16(128, 128, ab, 0, 0);   // S^T, dP^T (both operands K-major)
     constexpr uint32_t idKV = idesc_f16(128, 64, ab, 0, 1);    // dV, dK (A K-major or in tensor memory, B MN-major)
     constexpr uint32_t idQ = idesc_f16(128, 64, ab, 1, 1);     // dQ (A MN-major, B MN-major)
-    const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
     const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
     const uint32_t sDS = smem_u32(smem + L::kDS);
+    ItemSeq seq{(int)blockIdx.x, (int)gridDim.x, total, 0};
     if (warp == 16) {
       // ===================== TMA producer + dQ reduce =====================
-      // Loads of step t and the reduce of the staged dQ of step t - kLag run
-      // interleaved in one thread: the reduce of step r can only be staged
-      // after the load of step r + 1, and the load of step t needs, through
-      // the compute chain, the reduce of step t - 6, so this order never
-      // waits on itself; with the ring three steps deep each wait falls due
-      // at about the time the thread reaches it.
-      if (lane == 0 && n > 0) {
-        constexpr int kLag = 3;
+      // The loads of step g and the reduce of the staged dQ of step g - kLag
+      // run interleaved in one thread.  The reduce of step r can only be
+      // staged after the load of step r + 1, and the load of step g needs,
+      // through the compute chain, the reduce of step g - 5; so this order
+      // never waits on itself.
+      if (lane == 0) {
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmDO);
         prefetch_tmap(&tmDQ);
-        mbar_expect_tx(&bars->kv_full, 32768);
-        tma_load_4d(smem + L::kK, &tmK, &bars->kv_full, 0, jt * kTile, hk, b);
-        tma_load_4d(smem + L::kV, &tmV, &bars->kv_full, 0, jt * kTile, hk, b);
-        int issued = 0;
+        int4* info = reinterpret_cast<int4*>(smem + L::kInfo);
+        int g = 0, nkv = 0;
         bool ok = true;
-        int qu = 0, hq = ql.h0;      // load side: tile within query head hq
-        int rqu = 0, rhq = ql.h0;    // reduce side
-        for (int t = 0; t < n + kLag && ok; ++t) {
-          if (t < n) {
-            const int st = t % NSB;
-            const uint32_t ph = (uint32_t)(t / NSB) & 1u;
-            if (!(ok = mbar_wait(&bars->q_empty[st], ph ^ 1u, ctl))) break;
-            const int qi = ql.list ? (int)ql.list[qu] : ql.i0 + qu;
-            const size_t ld_row = ((size_t)b * a.H + hq) * a.npad + (size_t)qi * kTile;
+        auto reduce = [&](int r) -> bool {
+          const int bi = r % NSTG;
+          if (!mbar_wait(&bars->stg_full[bi], (uint32_t)(r / NSTG) & 1u, ctl)) return false;
+          const uint8_t* sb = smem + L::kDQ + bi * 32768;
+          const int4 inf = info[r & 3];
+          tma_reduce_add_4d(&tmDQ, sb, 0, inf.x * kTile, inf.y, inf.z);
+          tma_reduce_add_4d(&tmDQ, sb + 16384, 32, inf.x * kTile, inf.y, inf.z);
+          bulk_commit();
+          bulk_wait_read0();
+          mbar_arrive(&bars->stg_free[bi]);
+          return true;
+        };
+        int u;
+        while (ok && seq.next(u)) {
+          const Item it = make_item(a, u);
+          if (it.steps == 0) continue;
+          const int kb = nkv & 1;
+          if (!(ok = mbar_wait(&bars->kv_empty[kb], ((uint32_t)(nkv >> 1) & 1u) ^ 1u, ctl))) break;
+          mbar_expect_tx(&bars->kv_full[kb], 32768);
+          tma_load_4d(smem + L::kK + kb * 16384, &tmK, &bars->kv_full[kb], 0, it.jt * kTile, it.hk, it.b);
+          tma_load_4d(smem + L::kV + kb * 16384, &tmV, &bars->kv_full[kb], 0, it.jt * kTile, it.hk, it.b);
+          ++nkv;
+          int qu = 0, hq = it.h0;
+          for (int t = 0; t < it.steps && ok; ++t, ++g) {
+            const int st = g % NSB;
+            if (!(ok = mbar_wait(&bars->q_empty[st], ((uint32_t)(g / NSB) & 1u) ^ 1u, ctl))) break;
+            const int qi = it.qt(qu);
+            const size_t ld_row = ((size_t)it.b * a.H + hq) * a.npad + (size_t)qi * kTile;
             mbar_expect_tx(&bars->q_full[st], 32768 + 1024);
-            tma_load_4d(smem + L::kQ + st * 16384, &tmQ, &bars->q_full[st], 0, qi * kTile, hq, b);
-            tma_load_4d(smem + L::kDO + st * 16384, &tmDO, &bars->q_full[st], 0, qi * kTile, hq, b);
+            tma_load_4d(smem + L::kQ + st * 16384, &tmQ, &bars->q_full[st], 0, qi * kTile, hq, it.b);
+            tma_load_4d(smem + L::kDO + st * 16384, &tmDO, &bars->q_full[st], 0, qi * kTile, hq, it.b);
             bulk_load(smem + L::kLD + st * 1024, a.lse2 + ld_row, 512, &bars->q_full[st]);
             bulk_load(smem + L::kLD + st * 1024 + 512, a.dvec + ld_row, 512, &bars->q_full[st]);
-            ++issued;
-            if (++qu == ql.n) { qu = 0; ++hq; }
-          }
-          const int r = t - kLag;
-          if (r >= 0 && r < n) {
-            // staging buffer r % NSTG -> two TMA reduce-adds into the float32 accumulator
-            const int bi = r % NSTG;
-            if (!(ok = mbar_wait(&bars->stg_full[bi], (uint32_t)(r / NSTG) & 1u, ctl))) break;
-            const uint8_t* sb = smem + L::kDQ + bi * 32768;
-            const int qi = ql.list ? (int)ql.list[rqu] : ql.i0 + rqu;
-            tma_reduce_add_4d(&tmDQ, sb, 0, qi * kTile, rhq, b);
-            tma_reduce_add_4d(&tmDQ, sb + 16384, 32, qi * kTile, rhq, b);
-            bulk_commit();
-            if (++rqu == ql.n) { rqu = 0; ++rhq; }
-            bulk_wait_read0();
-            mbar_arrive(&bars->stg_free[bi]);
+            info[g & 3] = make_int4(qi, hq, it.b, 0);
+            if (++qu == it.n) { qu = 0; ++hq; }
+            if (g >= kLag && !(ok = reduce(g - kLag))) break;
           }
         }
-        for (int t = max(0, issued - NSB); t < issued; ++t)
-          mbar_wait(&bars->q_full[t % NSB], (uint32_t)(t / NSB) & 1u, ctl);
-        mbar_wait(&bars->kv_full, 0, ctl);
+        // the reduces still owed, then no copy may still be in flight
+        if (ok)
+          for (int r = max(0, g - kLag); r < g && ok; ++r) ok = reduce(r);
+        for (int t = max(0, g - NSB); t < g; ++t) mbar_wait(&bars->q_full[t % NSB], (uint32_t)(t / NSB) & 1u, ctl);
+        for (int t = max(0, nkv - 2); t < nkv; ++t) mbar_wait(&bars->kv_full[t & 1], (uint32_t)(t >> 1) & 1u, ctl);
         bulk_wait_read0();
       }
     } else if (warp == 17) {
       // ===================== S^T / dP^T issuer =====================
-      if (lane == 0 && n > 0) {
-        auto issue_sd = [&](uint32_t col, uint32_t sA, uint32_t sB) {   // col = sA sB^T, K-dim = d
+      if (lane == 0) {
+        int g = 0, nkv = 0;
+        bool ok = true;
+        int u;
+        while (ok && seq.next(u)) {
+          const Item it = make_item(a, u);
+          if (it.steps == 0) continue;
+          const int kb = nkv & 1;
+          if (!(ok = mbar_wait(&bars->kv_full[kb], (uint32_t)(nkv >> 1) & 1u, ctl))) break;
+          ++nkv;
+          const uint32_t sK = smem_u32(smem + L::kK + kb * 16384), sV = smem_u32(smem + L::kV + kb * 16384);
+          for (int t = 0; t < it.steps && ok; ++t, ++g) {
+            const int st = g % NSB;
+            // S^T(g) = K Q_g^T once part 1 of step g-1 has read S^T(g-1)
+            if (g > 0 && !(ok = mbar_wait(&bars->p_full, (uint32_t)(g - 1) & 1u, ctl))) break;
+            if (!(ok = mbar_wait(&bars->q_full[st], (uint32_t)(g / NSB) & 1u, ctl))) break;
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + col, sdesc_sw128(sA + k * 32, 16, 1024), sdesc_sw128(sB + k * 32, 16, 1024), idST,
-                   k > 0 ? 1u : 0u);
-        };
-        bool ok = mbar_wait(&bars->kv_full, 0, ctl) && mbar_wait(&bars->q_full[0], 0, ctl);
-        if (ok) {
-          tc_fence_after();
-          issue_sd(kColST, sK, sQ);
-          mma_commit(&bars->s_full);
-          issue_sd(kColDP, sV, sDO);
-          mma_commit(&bars->dp_full);
-        }
-        for (int t = 0; t + 1 < n && ok; ++t) {
-          const int st1 = (t + 1) % NSB;
-          // S^T(t+1) = K Q_{t+1}^T once part 1 of step t has read S^T(t)
-          if (!(ok = mbar_wait(&bars->p_full, (uint32_t)t & 1u, ctl) &&
-                     mbar_wait(&bars->q_full[st1], (uint32_t)((t + 1) / NSB) & 1u, ctl))) break;
-          tc_fence_after();
-          issue_sd(kColST, sK, sQ + st1 * 16384);
-          mma_commit(&bars->s_full);
-          // dP^T(t+1) = V dO_{t+1}^T once part 2 of step t has read dP^T(t)
-          if (!(ok = mbar_wait(&bars->ds_full, (uint32_t)t & 1u, ctl))) break;
-          tc_fence_after();
-          issue_sd(kColDP, sV, sDO + st1 * 16384);
-          mma_commit(&bars->dp_full);
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + kColST, sdesc_sw128(sK + k * 32, 16, 1024), sdesc_sw128(sQ + st * 16384 + k * 32, 16, 1024),
+                     idST, k > 0 ? 1u : 0u);
+            mma_commit(&bars->s_full);
+            // dP^T(g) = V dO_g^T once part 2 of step g-1 has read dP^T(g-1)
+            if (g > 0 && !(ok = mbar_wait(&bars->ds_full, (uint32_t)(g - 1) & 1u, ctl))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + kColDP, sdesc_sw128(sV + k * 32, 16, 1024), sdesc_sw128(sDO + st * 16384 + k * 32, 16, 1024),
+                     idST, k > 0 ? 1u : 0u);
+            mma_commit(&bars->dp_full);
+          }
+          mma_commit(&bars->kv_empty[kb]);   // this item's S^T and dP^T are done with K, V
         }
         mma_commit(&bars->done[0]);
         mbar_wait(&bars->done[0], 0, ctl);
       }
     } else if (warp == 18) {
       // ===================== dV / dK issuer =====================
-      if (lane == 0 && n > 0) {
+      // The first dV / dK of an item restart the accumulators; they follow
+      // p_full / ds_full of that step, which the compute warps arrive at only
+      // after reading the previous item's dK and dV out of tensor memory.
+      if (lane == 0) {
+        int g = 0;
         bool ok = true;
-        for (int t = 0; t < n && ok; ++t) {
-          const int st = t % NSB;
-          const uint32_t qb = sQ + st * 16384, db = sDO + st * 16384;
-          // dV += P~^T dO_t  (A = P~^T in tensor memory; K-dim = 128 queries, 8 steps of 16)
-          if (!(ok = mbar_wait(&bars->p_full, (uint32_t)t & 1u, ctl) &&
-                     mbar_wait(&bars->q_full[st], (uint32_t)(t / NSB) & 1u, ctl))) break;
-          tc_fence_after();
+        int u;
+        while (ok && seq.next(u)) {
+          const Item it = make_item(a, u);
+          if (it.steps == 0) continue;
+          for (int t = 0; t < it.steps && ok; ++t, ++g) {
+            const int st = g % NSB;
+            const uint32_t qb = sQ + st * 16384, db = sDO + st * 16384;
+            // dV += P~^T dO_g  (A = P~^T in tensor memory; K-dim = 128 queries, 8 steps of 16)
+            if (!(ok = mbar_wait(&bars->p_full, (uint32_t)g & 1u, ctl) &&
+                       mbar_wait(&bars->q_full[st], (uint32_t)(g / NSB) & 1u, ctl))) break;
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + kColDV, tmem + kColPT + k * 8, sdesc_sw128(db + k * 2048, 16384, 1024), idKV,
-                   (t > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&bars->pt_free);
-          // dK += dS^T Q_t  (A = dS^T from the shared tile, K-major: chunk k / 4, 32 bytes per 16 queries)
-          if (!(ok = mbar_wait(&bars->ds_full, (uint32_t)t & 1u, ctl))) break;
-          tc_fence_after();
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tmem + kColDV, tmem + kColPT + k * 8, sdesc_sw128(db + k * 2048, 16384, 1024), idKV,
+                     (t > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&bars->pt_free);
+            // dK += dS^T Q_g  (A = dS^T from the shared tile, K-major: chunk k / 4, 32 bytes per 16 queries)
+            if (!(ok = mbar_wait(&bars->ds_full, (uint32_t)g & 1u, ctl))) break;
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + kColDK, sdesc_sw128(sDS + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                   sdesc_sw128(qb + k * 2048, 16384, 1024), idKV, (t > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&bars->dsm_free);
-          mma_commit(&bars->q_empty[st]);
+            for (int k = 0; k < 8; ++k)
+              mma_ss(tmem + kColDK, sdesc_sw128(sDS + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                     sdesc_sw128(qb + k * 2048, 16384, 1024), idKV, (t > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&bars->dsm_free);
+            mma_commit(&bars->q_empty[st]);
+          }
+          mma_commit(&bars->dkv_full);       // this item's dK, dV are final
         }
-        mma_commit(&bars->dkv_full);
         mma_commit(&bars->done[1]);
         mbar_wait(&bars->done[1], 0, ctl);
       }
     } else {
       // ===================== dQ issuer (warp 19) =====================
-      if (lane == 0 && n > 0) {
+      if (lane == 0) {
+        int g = 0, nkv = 0;
         bool ok = true;
-        for (int t = 0; t < n && ok; ++t) {
-          // dQ_t = dS K  (M = 128 queries from the MN-major view of dS^T, K-dim = 128 keys)
-          if (!(ok = mbar_wait(&bars->ds_full, (uint32_t)t & 1u, ctl))) break;
-          if (t > 0 && !(ok = mbar_wait(&bars->dq_free, (uint32_t)(t - 1) & 1u, ctl))) break;
-          tc_fence_after();
+        int u;
+        while (ok && seq.next(u)) {
+          const Item it = make_item(a, u);
+          if (it.steps == 0) continue;
+          const int kb = nkv & 1;
+          ++nkv;
+          const uint32_t sK = smem_u32(smem + L::kK + kb * 16384);
+          for (int t = 0; t < it.steps && ok; ++t, ++g) {
+            // dQ_g = dS K  (M = 128 queries from the MN-major view of dS^T, K-dim = 128 keys)
+            if (!(ok = mbar_wait(&bars->ds_full, (uint32_t)g & 1u, ctl))) break;
+            if (g > 0 && !(ok = mbar_wait(&bars->dq_free, (uint32_t)(g - 1) & 1u, ctl))) break;
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + kColDQ, sdesc_sw128(sDS + k * 2048, 16384, 1024), sdesc_sw128(sK + k * 2048, 16384, 1024),
-                   idQ, k > 0 ? 1u : 0u);
-          mma_commit(&bars->dq_full);
-          mma_commit(&bars->dsm_free);
+            for (int k = 0; k < 8; ++k)
+              mma_ss(tmem + kColDQ, sdesc_sw128(sDS + k * 2048, 16384, 1024),
+                     sdesc_sw128(sK + k * 2048, 16384, 1024), idQ, k > 0 ? 1u : 0u);
+            mma_commit(&bars->dq_full);
+            mma_commit(&bars->dsm_free);
+          }
+          mma_commit(&bars->kv_empty[kb]);   // this item's dQ MMAs are done with K
         }
         mma_commit(&bars->done[2]);
         mbar_wait(&bars->done[2], 0, ctl);
@@ -327,10 +393,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int wg = warp >> 2;                 // query columns 32 wg .. 32 wg + 31
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;        // key row within the tile = TMEM lane
-    const int j = jt * kTile + r;             // global key
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tl = tmem + lane_off;
-    const bool key_ok = j < Lk;
     const float sl2 = a.scale_log2;
     const int c0 = wg * 32;                   // first query column of this warpgroup
     // 16-byte pieces (w & 1) * 4 .. + 4 of a 128-byte swizzled row belong to this warpgroup
@@ -365,192 +429,198 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       return true;
     };
 
-    // qu: tile position within the current query head qh (step t = (qh - h0) * ql.n + qu)
-    int qu = 0, qh = ql.h0;
-    for (int t = 0; t < n && ok; ++t, qu = (qu + 1 == ql.n) ? 0 : qu + 1, qh += (qu == 0) ? 1 : 0) {
+
+    // dK (x tau) and dV of an item: 16 of the 64 columns of this thread's key
+    // row, straight from registers to global memory (32 bytes each).
+    auto store_dkv = [&](const Item& it, const uint32_t (&kraw)[16], const uint32_t (&vraw)[16], bool have) {
+      const int j = it.jt * kTile + r;
+      if (j >= a.N) return;
+      const size_t off = (size_t)it.b * a.kst.b + (size_t)it.hk * a.kst.h + (size_t)j * a.kst.n + wg * 16;
+      uint32_t wk[8], wv[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        wk[c] = Cvt<T>::pack(have ? __uint_as_float(kraw[2 * c]) * a.scale : 0.f,
+                             have ? __uint_as_float(kraw[2 * c + 1]) * a.scale : 0.f);
+        wv[c] = Cvt<T>::pack(have ? __uint_as_float(vraw[2 * c]) : 0.f, have ? __uint_as_float(vraw[2 * c + 1]) : 0.f);
+      }
+      uint4* dk = reinterpret_cast<uint4*>(static_cast<T*>(a.dk) + off);
+      uint4* dv = reinterpret_cast<uint4*>(static_cast<T*>(a.dv) + off);
+      dk[0] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+      dk[1] = make_uint4(wk[4], wk[5], wk[6], wk[7]);
+      dv[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      dv[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+    };
+
+    ItemSeq seq{(int)blockIdx.x, (int)gridDim.x, total, 0};
+    int t = 0;        // global step
+    int nit = 0;      // items with steps (dkv_full phases)
+    int u;
+    while (ok && seq.next(u)) {
+      const Item it = make_item(a, u);
+      const uint32_t zero[16] = {};
+      if (it.steps == 0) {            // no query tile sees this key tile: dK = dV = 0
+        store_dkv(it, zero, zero, false);
+        continue;
+      }
+      const int j = it.jt * kTile + r;          // global key
+      const bool key_ok = j < it.Lk;
+      // qu: tile position within the current query head qh of the item;
+      // t: the global step (across items), which every ring and phase follows
+      int qu = 0, qh = it.h0;
+      for (int tt = 0; tt < it.steps && ok; ++tt, ++t, qu = (qu + 1 == it.n) ? 0 : qu + 1, qh += (qu == 0) ? 1 : 0) {
       const int st = t % NSB;
-      const int qi = ql.list ? (int)ql.list[qu] : ql.i0 + qu;
-      const uint32_t bh_rows = ((uint32_t)b * (uint32_t)a.H + (uint32_t)qh) * (uint32_t)a.N;
-      // LSE*log2e and D of this warpgroup's 32 query columns, in shared memory
-      const uint32_t s_lse = smem_u32(smem + L::kLD + st * 1024) + c0 * 4;
-      const uint32_t s_d = s_lse + 512;
-      // query column c of the tile is hidden from this key under causal iff
-      // c < qlo, and outside its sliding window iff c >= qhe
-      const int qlo = a.mask.causal ? (j - qi * kTile) : -1;
-      const int qhe = kWin ? (j + a.mask.window - qi * kTile) : kTile;
-      const bool any_mask = !key_ok || qlo > c0 || (kWin && qhe < c0 + 32);
+      const int qi = it.qt(qu);
+      const uint32_t bh_rows = ((uint32_t)it.b * (uint32_t)a.H + (uint32_t)qh) * (uint32_t)a.N;
+        // LSE*log2e and D of this warpgroup's 32 query columns, in shared memory
+        const uint32_t s_lse = smem_u32(smem + L::kLD + st * 1024) + c0 * 4;
+        const uint32_t s_d = s_lse + 512;
+        // query column c of the tile is hidden from this key under causal iff
+        // c < qlo, and outside its sliding window iff c >= qhe
+        const int qlo = a.mask.causal ? (j - qi * kTile) : -1;
+        const int qhe = kWin ? (j + a.mask.window - qi * kTile) : kTile;
+        const bool any_mask = !key_ok || qlo > c0 || (kWin && qhe < c0 + 32);
 
-      // ---- part 1: P from S^T, in two halves of 16 query columns; the
-      //      tensor-memory load of the second half overlaps the first's math
-      if (!(ok = warp_wait(&bars->s_full, (uint32_t)t & 1u, ctl) &&
-                 warp_wait(&bars->q_full[st], (uint32_t)(t / NSB) & 1u, ctl))) break;
-      tc_fence_after();
-      uint32_t sv[2][16];
-      tmem_ld16(tl + kColST + c0, sv[0]);
-      uint32_t keep = ~0u;
-      if constexpr (kDrop) {
-        // One Philox call covers 8 consecutive keys of one query row, and the
-        // 8 lanes 8m..8m+7 hold 8 consecutive keys (j & 7 == lane & 7).  So
-        // lane t of each group evaluates the calls of queries t, t+8, t+16,
-        // t+24 (4 instead of 32), packs their 8-key keep bytes into one word,
-        // and the group exchanges the words.
-        const int t8 = lane & 7;
-        uint32_t mine = 0;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const uint32_t q = (uint32_t)(qi * kTile + c0 + t8 + 8 * m);
-          mine |= dropout_keep8((uint32_t)j >> 3, bh_rows + q, a.drop) << (8 * m);
-        }
-        uint32_t kb = 0;
-#pragma unroll
-        for (int src = 0; src < 8; ++src) {
-          const uint32_t w = __shfl_sync(0xffffffffu, mine, (lane & ~7) | src);
-#pragma unroll
-          for (int m = 0; m < 4; ++m) kb |= ((w >> (8 * m + t8)) & 1u) << (src + 8 * m);
-        }
-        keep = kb;
-      }
-      uint32_t pp[16];      // undropped P, 16 bit, kept for part 2
-      uint32_t pt[16];      // P~ = Z o P / (1 - p), 16 bit, operand of dV
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        tmem_wait_ld();
-        reg_fence16(sv[hf]);
-        if (hf == 0) tmem_ld16(tl + kColST + c0 + 16, sv[1]);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int cc = hf * 16 + q4 * 4;    // column within this warpgroup's 32
-          const float4 l4 = lds128(s_lse + cc * 4);
-          float x[4];
-          fma2(x[0], x[1], __uint_as_float(sv[hf][q4 * 4]), __uint_as_float(sv[hf][q4 * 4 + 1]), sl2, sl2, -l4.x, -l4.y);
-          fma2(x[2], x[3], __uint_as_float(sv[hf][q4 * 4 + 2]), __uint_as_float(sv[hf][q4 * 4 + 3]), sl2, sl2, -l4.z, -l4.w);
-          float p[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) p[e] = ex2(x[e]);
-          if (any_mask) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (!key_ok || c0 + cc + e < qlo || (kWin && c0 + cc + e >= qhe)) p[e] = 0.f;
-          }
-          const uint32_t w0 = Cvt<T>::pack(p[0], p[1]), w1 = Cvt<T>::pack(p[2], p[3]);
-          pp[cc / 2] = w0;
-          pp[cc / 2 + 1] = w1;
-          if constexpr (kDrop) {
-            const uint32_t kb = keep >> cc;
-            const float rp = a.drop.rp;
-            pt[cc / 2] = Cvt<T>::pack((kb & 1u) ? p[0] * rp : 0.f, (kb & 2u) ? p[1] * rp : 0.f);
-            pt[cc / 2 + 1] = Cvt<T>::pack((kb & 4u) ? p[2] * rp : 0.f, (kb & 8u) ? p[3] * rp : 0.f);
-          } else {
-            pt[cc / 2] = w0;
-            pt[cc / 2 + 1] = w1;
-          }
-        }
-      }
-      // dV of the previous step must have read P~^T
-      if (t > 0 && !(ok = warp_wait(&bars->pt_free, (uint32_t)(t - 1) & 1u, ctl))) break;
-      tmem_st16(tl + kColPT + wg * 16, pt);
-      // dP^T(t) is usually complete by now: start its first load before the store is waited on
-      if (!(ok = warp_wait(&bars->dp_full, (uint32_t)t & 1u, ctl))) break;
-      tc_fence_after();
-      uint32_t dv[2][16];
-      tmem_ld16(tl + kColDP + c0, dv[0]);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full);
-
-      // ---- part 2: dS from dP^T, in the same two halves
-      // dS^T also goes to the shared tile, once dQ of the previous step has read it
-      if (t >= 1 && !(ok = warp_wait(&bars->dsm_free, (uint32_t)(t - 1) & 1u, ctl))) break;
-      uint8_t* dsb = smem + L::kDS + (wg >> 1) * 16384 + r * 128;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        tmem_wait_ld();
-        reg_fence16(dv[hf]);
-        if (hf == 0) tmem_ld16(tl + kColDP + c0 + 16, dv[1]);
-        uint32_t dsw[8];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int cc = hf * 16 + q4 * 4;
-          const float4 d4 = lds128(s_d + cc * 4);
-          float g[4] = {__uint_as_float(dv[hf][q4 * 4]), __uint_as_float(dv[hf][q4 * 4 + 1]),
-                        __uint_as_float(dv[hf][q4 * 4 + 2]), __uint_as_float(dv[hf][q4 * 4 + 3])};
-          if constexpr (kDrop) {
-            const uint32_t kb = keep >> cc;
-            const float rp = a.drop.rp;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) g[e] = ((kb >> e) & 1u) ? g[e] * rp : 0.f;
-          }
-          const uint32_t w0 = pp[cc / 2], w1 = pp[cc / 2 + 1];
-          float y[4];
-          sub2(y[0], y[1], g[0], g[1], d4.x, d4.y);
-          sub2(y[2], y[3], g[2], g[3], d4.z, d4.w);
-          mul2(y[0], y[1], y[0], y[1], Cvt<T>::lo(w0), Cvt<T>::hi(w0));
-          mul2(y[2], y[3], y[2], y[3], Cvt<T>::lo(w1), Cvt<T>::hi(w1));
-          dsw[q4 * 2] = Cvt<T>::pack(y[0], y[1]);
-          dsw[q4 * 2 + 1] = Cvt<T>::pack(y[2], y[3]);
-        }
-#pragma unroll
-        for (int pc2 = 0; pc2 < 2; ++pc2) {
-          const uint32_t off = ((((pc_base + hf * 2 + pc2) ^ r) & 7) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                       :: "r"(smem_u32(dsb + off)), "r"(dsw[pc2 * 4]), "r"(dsw[pc2 * 4 + 1]), "r"(dsw[pc2 * 4 + 2]),
-                          "r"(dsw[pc2 * 4 + 3]) : "memory");
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars->ds_full);
-
-      // ---- drain dQ of the previous step
-      if (t > 0 && !(ok = drain_dq(t - 1))) break;
-    }
-    if (ok && n > 0) ok = drain_dq(n - 1);
-
-    // ---- epilogue: 16 of the 64 columns of dK (x tau) and dV -> 16 bit ->
-    //      shared -> TMA store
-    if (!named_bar_or(1, kCompute, !ok || bars->abort)) {
-      uint32_t kraw[16], vraw[16];
-      bool have = false;
-      if (n > 0 && warp_wait(&bars->dkv_full, 0, ctl)) {
+        // ---- part 1: P from S^T, in two halves of 16 query columns; the
+        //      tensor-memory load of the second half overlaps the first's math
+        if (!(ok = warp_wait(&bars->s_full, (uint32_t)t & 1u, ctl) &&
+                   warp_wait(&bars->q_full[st], (uint32_t)(t / NSB) & 1u, ctl))) break;
         tc_fence_after();
-        tmem_ld16(tl + kColDK + wg * 16, kraw);
-        tmem_ld16(tl + kColDV + wg * 16, vraw);
-        tmem_wait_ld();
-        reg_fence16(kraw);
-        reg_fence16(vraw);
-        have = true;
-      }
-      uint8_t* kb = smem + L::kDS;          // dS^T buffers are dead after dkv_full
-      uint8_t* vb = smem + L::kDS + 16384;
-#pragma unroll
-      for (int pc2 = 0; pc2 < 2; ++pc2) {
-        const int pc = wg * 2 + pc2;        // 16-byte piece = 8 columns
-        uint32_t wk[4], wv[4];
-#pragma unroll
-        for (int t2 = 0; t2 < 4; ++t2) {
-          const int c = pc2 * 8 + 2 * t2;   // column within this warpgroup's 16
-          const float k0 = have ? __uint_as_float(kraw[c]) * a.scale : 0.f;
-          const float k1 = have ? __uint_as_float(kraw[c + 1]) * a.scale : 0.f;
-          const float v0 = have ? __uint_as_float(vraw[c]) : 0.f;
-          const float v1 = have ? __uint_as_float(vraw[c + 1]) : 0.f;
-          wk[t2] = Cvt<T>::pack(k0, k1);
-          wv[t2] = Cvt<T>::pack(v0, v1);
+        uint32_t sv[2][16];
+        tmem_ld16(tl + kColST + c0, sv[0]);
+        uint32_t keep = ~0u;
+        if constexpr (kDrop) {
+          // One Philox call covers 8 consecutive keys of one query row, and the
+          // 8 lanes 8m..8m+7 hold 8 consecutive keys (j & 7 == lane & 7).  So
+          // lane t of each group evaluates the calls of queries t, t+8, t+16,
+          // t+24 (4 instead of 32), packs their 8-key keep bytes into one word,
+          // and the group exchanges the words.
+          const int t8 = lane & 7;
+          uint32_t mine = 0;
+  #pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t q = (uint32_t)(qi * kTile + c0 + t8 + 8 * m);
+            mine |= dropout_keep8((uint32_t)j >> 3, bh_rows + q, a.drop) << (8 * m);
+          }
+          uint32_t kb = 0;
+  #pragma unroll
+          for (int src = 0; src < 8; ++src) {
+            const uint32_t w = __shfl_sync(0xffffffffu, mine, (lane & ~7) | src);
+  #pragma unroll
+            for (int m = 0; m < 4; ++m) kb |= ((w >> (8 * m + t8)) & 1u) << (src + 8 * m);
+          }
+          keep = kb;
         }
-        const uint32_t off = r * 128 + (((pc ^ r) & 7) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                     :: "r"(smem_u32(kb + off)), "r"(wk[0]), "r"(wk[1]), "r"(wk[2]), "r"(wk[3]) : "memory");
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                     :: "r"(smem_u32(vb + off)), "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3]) : "memory");
+        uint32_t pp[16];      // undropped P, 16 bit, kept for part 2
+        uint32_t pt[16];      // P~ = Z o P / (1 - p), 16 bit, operand of dV
+  #pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          tmem_wait_ld();
+          reg_fence16(sv[hf]);
+          if (hf == 0) tmem_ld16(tl + kColST + c0 + 16, sv[1]);
+  #pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int cc = hf * 16 + q4 * 4;    // column within this warpgroup's 32
+            const float4 l4 = lds128(s_lse + cc * 4);
+            float x[4];
+            fma2(x[0], x[1], __uint_as_float(sv[hf][q4 * 4]), __uint_as_float(sv[hf][q4 * 4 + 1]), sl2, sl2, -l4.x, -l4.y);
+            fma2(x[2], x[3], __uint_as_float(sv[hf][q4 * 4 + 2]), __uint_as_float(sv[hf][q4 * 4 + 3]), sl2, sl2, -l4.z, -l4.w);
+            float p[4];
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) p[e] = ex2(x[e]);
+            if (any_mask) {
+  #pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (!key_ok || c0 + cc + e < qlo || (kWin && c0 + cc + e >= qhe)) p[e] = 0.f;
+            }
+            const uint32_t w0 = Cvt<T>::pack(p[0], p[1]), w1 = Cvt<T>::pack(p[2], p[3]);
+            pp[cc / 2] = w0;
+            pp[cc / 2 + 1] = w1;
+            if constexpr (kDrop) {
+              const uint32_t kb = keep >> cc;
+              const float rp = a.drop.rp;
+              pt[cc / 2] = Cvt<T>::pack((kb & 1u) ? p[0] * rp : 0.f, (kb & 2u) ? p[1] * rp : 0.f);
+              pt[cc / 2 + 1] = Cvt<T>::pack((kb & 4u) ? p[2] * rp : 0.f, (kb & 8u) ? p[3] * rp : 0.f);
+            } else {
+              pt[cc / 2] = w0;
+              pt[cc / 2 + 1] = w1;
+            }
+          }
+        }
+        // dV of the previous step must have read P~^T
+        if (t > 0 && !(ok = warp_wait(&bars->pt_free, (uint32_t)(t - 1) & 1u, ctl))) break;
+        tmem_st16(tl + kColPT + wg * 16, pt);
+        // dP^T(t) is usually complete by now: start its first load before the store is waited on
+        if (!(ok = warp_wait(&bars->dp_full, (uint32_t)t & 1u, ctl))) break;
+        tc_fence_after();
+        uint32_t dv[2][16];
+        tmem_ld16(tl + kColDP + c0, dv[0]);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full);
+
+        // ---- part 2: dS from dP^T, in the same two halves
+        // dS^T also goes to the shared tile, once dQ of the previous step has read it
+        if (t >= 1 && !(ok = warp_wait(&bars->dsm_free, (uint32_t)(t - 1) & 1u, ctl))) break;
+        uint8_t* dsb = smem + L::kDS + (wg >> 1) * 16384 + r * 128;
+  #pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          tmem_wait_ld();
+          reg_fence16(dv[hf]);
+          if (hf == 0) tmem_ld16(tl + kColDP + c0 + 16, dv[1]);
+          uint32_t dsw[8];
+  #pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int cc = hf * 16 + q4 * 4;
+            const float4 d4 = lds128(s_d + cc * 4);
+            float g[4] = {__uint_as_float(dv[hf][q4 * 4]), __uint_as_float(dv[hf][q4 * 4 + 1]),
+                          __uint_as_float(dv[hf][q4 * 4 + 2]), __uint_as_float(dv[hf][q4 * 4 + 3])};
+            if constexpr (kDrop) {
+              const uint32_t kb = keep >> cc;
+              const float rp = a.drop.rp;
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) g[e] = ((kb >> e) & 1u) ? g[e] * rp : 0.f;
+            }
+            const uint32_t w0 = pp[cc / 2], w1 = pp[cc / 2 + 1];
+            float y[4];
+            sub2(y[0], y[1], g[0], g[1], d4.x, d4.y);
+            sub2(y[2], y[3], g[2], g[3], d4.z, d4.w);
+            mul2(y[0], y[1], y[0], y[1], Cvt<T>::lo(w0), Cvt<T>::hi(w0));
+            mul2(y[2], y[3], y[2], y[3], Cvt<T>::lo(w1), Cvt<T>::hi(w1));
+            dsw[q4 * 2] = Cvt<T>::pack(y[0], y[1]);
+            dsw[q4 * 2 + 1] = Cvt<T>::pack(y[2], y[3]);
+          }
+  #pragma unroll
+          for (int pc2 = 0; pc2 < 2; ++pc2) {
+            const uint32_t off = ((((pc_base + hf * 2 + pc2) ^ r) & 7) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         :: "r"(smem_u32(dsb + off)), "r"(dsw[pc2 * 4]), "r"(dsw[pc2 * 4 + 1]), "r"(dsw[pc2 * 4 + 2]),
+                            "r"(dsw[pc2 * 4 + 3]) : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars->ds_full);
+
+        // ---- drain dQ of the previous step
+        if (t > 0 && !(ok = drain_dq(t - 1))) break;
       }
-      fence_proxy_async_smem();
-      named_bar_sync(1, kCompute);
-      if (threadIdx.x == 0) {
-        tma_store_4d(&tmDK, kb, 0, jt * kTile, hk, b);
-        tma_store_4d(&tmDV, vb, 0, jt * kTile, hk, b);
-        bulk_commit();
-        bulk_wait_read0();   // shared memory must outlive the reads; the writes finish with the grid
-      }
+      if (!ok) break;
+      // ---- item end: dK, dV out of tensor memory.  The next item's first
+      //      dV / dK (which restart the accumulators) follow this thread's
+      //      next p_full / ds_full arrivals, hence these loads.
+      uint32_t kraw[16], vraw[16];
+      if (!(ok = warp_wait(&bars->dkv_full, (uint32_t)nit & 1u, ctl))) break;
+      ++nit;
+      tc_fence_after();
+      tmem_ld16(tl + kColDK + wg * 16, kraw);
+      tmem_ld16(tl + kColDV + wg * 16, vraw);
+      tmem_wait_ld();
+      reg_fence16(kraw);
+      reg_fence16(vraw);
+      tc_fence_before();
+      store_dkv(it, kraw, vraw, true);
     }
+    if (ok && t > 0) ok = drain_dq(t - 1);
   }
 
   tc_fence_before();
@@ -563,37 +633,39 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
 template <typename T, bool kDrop, bool kWin>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
-                     const CUtensorMap& dk, const CUtensorMap& dv, const CUtensorMap& dqacc, const BwdArgs& a,
-                     cudaStream_t s) {
+                     const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s) {
   auto kern = bwd_tc_kernel<T, kDrop, kWin>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem::kDyn);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(a.nq * a.B * a.H_kv);
-  if (grid == 0) return cudaSuccess;
-  kern<<<grid, kThreads, BwdSmem::kDyn, s>>>(q, k, v, dout, dk, dv, dqacc, a);
+  const long long total = (long long)a.nq * a.B * a.H_kv;
+  if (total == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const unsigned grid = (unsigned)std::min<long long>(total, (long long)std::max(sms, 1));
+  kern<<<grid, kThreads, BwdSmem::kDyn, s>>>(q, k, v, dout, dqacc, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
-                          const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s) {
+                          const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s) {
   const int sel = (a.drop.enabled ? 1 : 0) | (a.mask.window > 0 ? 2 : 0);
   if (dtype == FA_DT_BF16) {
     using B = __nv_bfloat16;
     switch (sel) {
-      case 0: return launch_t<B, false, false>(q, k, v, dout, dk, dv, dqacc, a, s);
-      case 1: return launch_t<B, true, false>(q, k, v, dout, dk, dv, dqacc, a, s);
-      case 2: return launch_t<B, false, true>(q, k, v, dout, dk, dv, dqacc, a, s);
-      default: return launch_t<B, true, true>(q, k, v, dout, dk, dv, dqacc, a, s);
+      case 0: return launch_t<B, false, false>(q, k, v, dout, dqacc, a, s);
+      case 1: return launch_t<B, true, false>(q, k, v, dout, dqacc, a, s);
+      case 2: return launch_t<B, false, true>(q, k, v, dout, dqacc, a, s);
+      default: return launch_t<B, true, true>(q, k, v, dout, dqacc, a, s);
     }
   }
   switch (sel) {
-    case 0: return launch_t<__half, false, false>(q, k, v, dout, dk, dv, dqacc, a, s);
-    case 1: return launch_t<__half, true, false>(q, k, v, dout, dk, dv, dqacc, a, s);
-    case 2: return launch_t<__half, false, true>(q, k, v, dout, dk, dv, dqacc, a, s);
-    default: return launch_t<__half, true, true>(q, k, v, dout, dk, dv, dqacc, a, s);
+    case 0: return launch_t<__half, false, false>(q, k, v, dout, dqacc, a, s);
+    case 1: return launch_t<__half, true, false>(q, k, v, dout, dqacc, a, s);
+    case 2: return launch_t<__half, false, true>(q, k, v, dout, dqacc, a, s);
+    default: return launch_t<__half, true, true>(q, k, v, dout, dqacc, a, s);
   }
 }
 

@@ -15,6 +15,8 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr int kTile = 128;       // query rows (and key rows) per tile
 constexpr int kHeadDim = 64;     // head dimension handled by the kernels
 
+struct Strides { int64_t b, h, n; };
+
 struct DropoutArgs {
   uint32_t k0, k1;         // Philox key = (lo32(seed), hi32(seed))
   uint32_t off_lo, off_hi; // counter words 2, 3
@@ -59,6 +61,9 @@ struct BwdArgs {
   DropoutArgs drop;
   const float* lse2;          // [B*H][npad]: LSE*log2(e), +inf for rows without keys / padding
   const float* dvec;          // [B*H][npad]: D = rowsum(dO o O), 0 on padding
+  void* dk;                   // [B,H_kv,N,64] outputs, element strides kst
+  void* dv;
+  Strides kst;
   int* status;
 };
 
@@ -68,10 +73,7 @@ struct BwdArgs {
 cudaError_t launch_fwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& o, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
-                          const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s);
-
-struct Strides { int64_t b, h, n; };
+                          const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s);
 
 // st: strides of Q, O, dO, dQ ([B,H,N,d]); kst: strides of K, V, dK, dV ([B,H_kv,N,d]).
 cudaError_t launch_fwd_simt(const float* q, const float* k, const float* v, float* o, Strides st,
