@@ -34,7 +34,7 @@ EncodeTiledFn encode_fn() {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t status = 0, rlist = 0, rcnt = 0, clist = 0, ccnt = 0, lse2 = 0, dvec = 0, dqacc = 0, total = 0;
+  size_t status = 0, rlist = 0, rcnt = 0, clist = 0, ccnt = 0, lse2 = 0, dvec = 0, dqacc = 0, sched = 0, total = 0;
   bool sparse = false;
   int nb = 0, nq = 0, npad = 0;
 };
@@ -63,6 +63,7 @@ Layout layout(const fa_params* p, bool bwd) {
     L.lse2 = take(rows * sizeof(float));
     L.dvec = take(rows * sizeof(float));
     if (p->dtype != FA_DT_F32) L.dqacc = take((size_t)p->B * p->H * p->N * kHeadDim * sizeof(float));
+    L.sched = take(sizeof(int));
   }
   L.total = off;
   return L;
@@ -285,9 +286,10 @@ fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v
 
   if ((s = prepare_common(p, L, w, st)) != FA_OK) return s;
   float* dqacc = p->dtype == FA_DT_F32 ? nullptr : reinterpret_cast<float*>(w + L.dqacc);
+  a.sched = reinterpret_cast<int*>(w + L.sched);
   cudaError_t e = launch_bwd_prep(p->dtype, o, dout, sd, lse, p->B, p->H, p->N, L.npad,
                                   reinterpret_cast<float*>(w + L.lse2), reinterpret_cast<float*>(w + L.dvec), dqacc,
-                                  st);
+                                  a.sched, st);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   if (p->dtype == FA_DT_F32) {
     ProfScope prof(p, st);

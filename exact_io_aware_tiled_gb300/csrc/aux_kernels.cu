@@ -46,7 +46,9 @@ template <typename T> struct Vec8 {
 template <typename T>
 __global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ dout, Strides st,
                                 const float* __restrict__ lse, int B, int H, int N, int npad,
-                                float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dqacc) {
+                                float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dqacc,
+                                int* __restrict__ sched) {
+  if (sched != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;   // backward work counter
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 3;
   const int part = threadIdx.x & 7;
   const long long total = (long long)B * H * npad;
@@ -149,19 +151,19 @@ __global__ void dropout_mask_kernel(DropoutArgs d, int H, int N, int b, int h, i
 }  // namespace
 
 cudaError_t launch_bwd_prep(int dtype, const void* o, const void* dout, Strides st, const float* lse, int B, int H,
-                            int N, int npad, float* lse2, float* dvec, float* dqacc, cudaStream_t s) {
+                            int N, int npad, float* lse2, float* dvec, float* dqacc, int* sched, cudaStream_t s) {
   const long long rows = (long long)B * H * npad;
   const int threads = 256;
   const long long blocks = (rows * 8 + threads - 1) / threads;
   if (dtype == FA_DT_BF16)
     bwd_prep_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, s>>>(
-        (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, st, lse, B, H, N, npad, lse2, dvec, dqacc);
+        (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, st, lse, B, H, N, npad, lse2, dvec, dqacc, sched);
   else if (dtype == FA_DT_F16)
     bwd_prep_kernel<__half><<<(unsigned)blocks, threads, 0, s>>>((const __half*)o, (const __half*)dout, st, lse, B,
-                                                                 H, N, npad, lse2, dvec, dqacc);
+                                                                 H, N, npad, lse2, dvec, dqacc, sched);
   else
     bwd_prep_kernel<float><<<(unsigned)blocks, threads, 0, s>>>((const float*)o, (const float*)dout, st, lse, B, H,
-                                                                N, npad, lse2, dvec, dqacc);
+                                                                N, npad, lse2, dvec, dqacc, sched);
   return cudaGetLastError();
 }
 

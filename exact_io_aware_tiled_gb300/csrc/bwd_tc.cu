@@ -16,11 +16,12 @@
 // tiles that see a key tile and masks the window's far edge.
 //
 // GB300 mapping (ours): a persistent kernel, one CTA per SM.  The work items
-// are (b, K/V head, 128-key tile); CTA c takes, from each block of G
-// consecutive items (G = the grid), item (c + k) mod G of block k, so that
-// every CTA sees every key-tile position (the causal work per item varies
-// with it) while the CTAs working at one time cover a few adjacent heads,
-// whose Q / dO tiles and dQ accumulator rows stay in L2.  Per item the CTA
+// are (b, K/V head, 128-key tile) in head-major order; each CTA takes the
+// next one from a global counter as it goes (its producer thread fetches it
+// and hands it to the other roles through a two-slot shared-memory mailbox),
+// so CTAs that drew short items take more, and the CTAs working at one time
+// cover a few adjacent heads, whose Q / dO tiles and dQ accumulator rows
+// stay in L2.  Per item the CTA
 // loops over the query tiles that see the key tile, for each query head of
 // the group, so dK and dV accumulate over the group in tensor memory.  The
 // steps of consecutive items form one global sequence: every ring and
@@ -74,12 +75,14 @@ struct BwdSmem {
   static constexpr int kDQ = kDS + 32768;           // NSTG x 32 KB: float32 dQ staging [buf][half][128][32]
   static constexpr int kLD = kDQ + NSTG * 32768;    // NSB x (LSE2[128] + D[128]) floats
   static constexpr int kInfo = kLD + NSB * 1024;    // (query tile, query head, batch) of the last kLag+1 steps
-  static constexpr int kBar = kInfo + 64;
+  static constexpr int kItem = kInfo + 64;          // the two published work items
+  static constexpr int kBar = kItem + 64;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kDyn = kBytes + 1024;
 };
 
 struct BBars {
+  uint64_t item_full[2], item_empty[2];   // the work-item hand-off from warp 16 to the other roles
   uint64_t kv_full[2], kv_empty[2];
   uint64_t q_full[NSB], q_empty[NSB];
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free, dkv_full, pt_free;
@@ -141,23 +144,6 @@ __device__ __forceinline__ Item make_item(const BwdArgs& a, int u) {
   return it;
 }
 
-// The items of CTA c, in order: item (c + k) mod G of block k (items
-// k*G .. k*G + G - 1), skipping those past the end.
-struct ItemSeq {
-  int c, G, total, k;
-  __device__ __forceinline__ bool next(int& u) {
-    while (k * G < total) {
-      const int v = k * G + (c + k) % G;
-      ++k;
-      if (v < total) {
-        u = v;
-        return true;
-      }
-    }
-    return false;
-  }
-};
-
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
   const bool ok = mbar_wait(bar, parity, ctl);
   return __all_sync(0xffffffffu, ok);
@@ -181,6 +167,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->item_full[s], 1);
+      mbar_init(&bars->item_empty[s], 3 + kCompute);   // warps 17-19 and the compute threads
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 2);   // S/dP warp and dQ warp read K / V
     }
@@ -221,7 +209,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     constexpr uint32_t idQ = idesc_f16(128, 64, ab, 1, 1);     // dQ (A MN-major, B MN-major)
     const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
     const uint32_t sDS = smem_u32(smem + L::kDS);
-    ItemSeq seq{(int)blockIdx.x, (int)gridDim.x, total, 0};
+    volatile int* item_u = reinterpret_cast<volatile int*>(smem + L::kItem);
+    // the next work item from warp 16's mailbox (-1: no more, or a wait gave up)
+    int kc = 0;
+    auto fetch = [&]() -> int {
+      const int slot = kc & 1;
+      if (!mbar_wait(&bars->item_full[slot], (uint32_t)(kc >> 1) & 1u, ctl)) return -1;
+      const int v = item_u[slot];
+      mbar_arrive(&bars->item_empty[slot]);
+      ++kc;
+      return v;
+    };
     if (warp == 16) {
       // ===================== TMA producer + dQ reduce =====================
       // The loads of step g and the reduce of the staged dQ of step g - kLag
@@ -248,10 +246,42 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           mbar_arrive(&bars->stg_free[bi]);
           return true;
         };
+        // the next item from the global counter, handed to the other roles
+        // through the two-slot mailbox (-1: none left; -2: a wait gave up)
+        int kf = 0;
+        auto publish = [&]() -> int {
+          const int slot = kf & 1;
+          if (!mbar_wait(&bars->item_empty[slot], ((uint32_t)(kf >> 1) & 1u) ^ 1u, ctl)) return -2;
+          int v = atomicAdd(a.sched, 1);
+          if (v >= total) v = -1;
+          item_u[slot] = v;
+          mbar_arrive(&bars->item_full[slot]);
+          ++kf;
+          return v;
+        };
+        // reduces run in step order; rd is the next one owed
+        int rd = 0;
+        auto reduce_to = [&](int last) -> bool {
+          for (; rd <= last; ++rd)
+            if (!reduce(rd)) return false;
+          return true;
+        };
         int u;
-        while (ok && seq.next(u)) {
+        while (ok) {
+          u = publish();
+          if (u < 0) {
+            ok = u == -1;
+            break;
+          }
           const Item it = make_item(a, u);
-          if (it.steps == 0) continue;
+          if (it.steps == 0) {
+            // An empty item loads nothing, so the reduce that normally follows
+            // a load is not reached; do the reduces the compute threads need to
+            // finish their current item (through step g - 3), or a run of empty
+            // items would fill the mailbox while they wait for one.
+            ok = reduce_to(g - 3);
+            continue;
+          }
           const int kb = nkv & 1;
           if (!(ok = mbar_wait(&bars->kv_empty[kb], ((uint32_t)(nkv >> 1) & 1u) ^ 1u, ctl))) break;
           mbar_expect_tx(&bars->kv_full[kb], 32768);
@@ -271,12 +301,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             bulk_load(smem + L::kLD + st * 1024 + 512, a.dvec + ld_row, 512, &bars->q_full[st]);
             info[g & 3] = make_int4(qi, hq, it.b, 0);
             if (++qu == it.n) { qu = 0; ++hq; }
-            if (g >= kLag && !(ok = reduce(g - kLag))) break;
+            if (!(ok = reduce_to(g - kLag))) break;
           }
         }
         // the reduces still owed, then no copy may still be in flight
-        if (ok)
-          for (int r = max(0, g - kLag); r < g && ok; ++r) ok = reduce(r);
+        if (ok) ok = reduce_to(g - 1);
         for (int t = max(0, g - NSB); t < g; ++t) mbar_wait(&bars->q_full[t % NSB], (uint32_t)(t / NSB) & 1u, ctl);
         for (int t = max(0, nkv - 2); t < nkv; ++t) mbar_wait(&bars->kv_full[t & 1], (uint32_t)(t >> 1) & 1u, ctl);
         bulk_wait_read0();
@@ -287,7 +316,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         int g = 0, nkv = 0;
         bool ok = true;
         int u;
-        while (ok && seq.next(u)) {
+        while (ok && (u = fetch()) >= 0) {
           const Item it = make_item(a, u);
           if (it.steps == 0) continue;
           const int kb = nkv & 1;
@@ -328,7 +357,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         int g = 0;
         bool ok = true;
         int u;
-        while (ok && seq.next(u)) {
+        while (ok && (u = fetch()) >= 0) {
           const Item it = make_item(a, u);
           if (it.steps == 0) continue;
           for (int t = 0; t < it.steps && ok; ++t, ++g) {
@@ -364,7 +393,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         int g = 0, nkv = 0;
         bool ok = true;
         int u;
-        while (ok && seq.next(u)) {
+        while (ok && (u = fetch()) >= 0) {
           const Item it = make_item(a, u);
           if (it.steps == 0) continue;
           const int kb = nkv & 1;
@@ -451,11 +480,21 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       dv[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
     };
 
-    ItemSeq seq{(int)blockIdx.x, (int)gridDim.x, total, 0};
+    // the next work item from warp 16's mailbox (-1: none left, or a wait gave up)
+    volatile int* item_u = reinterpret_cast<volatile int*>(smem + L::kItem);
+    int kc = 0;
+    auto fetch = [&]() -> int {
+      const int slot = kc & 1;
+      if (!warp_wait(&bars->item_full[slot], (uint32_t)(kc >> 1) & 1u, ctl)) return -1;
+      const int v = item_u[slot];
+      mbar_arrive(&bars->item_empty[slot]);
+      ++kc;
+      return v;
+    };
     int t = 0;        // global step
     int nit = 0;      // items with steps (dkv_full phases)
     int u;
-    while (ok && seq.next(u)) {
+    while (ok && (u = fetch()) >= 0) {
       const Item it = make_item(a, u);
       const uint32_t zero[16] = {};
       if (it.steps == 0) {            // no query tile sees this key tile: dK = dV = 0

@@ -64,6 +64,7 @@ struct BwdArgs {
   void* dk;                   // [B,H_kv,N,64] outputs, element strides kst
   void* dv;
   Strides kst;
+  int* sched;                 // work-item counter of the persistent kernel (zeroed by the prepass)
   int* status;
 };
 
@@ -85,7 +86,7 @@ cudaError_t launch_bwd_simt(const float* q, const float* k, const float* v, cons
 // D = rowsum(dO o O) and the padded LSE*log2e / D arrays; the same pass clears dqacc if given.
 cudaError_t launch_bwd_prep(int dtype, const void* o, const void* dout, Strides st, const float* lse,
                             int B, int H, int N, int npad, float* lse2, float* dvec, float* dqacc,
-                            cudaStream_t s);
+                            int* sched, cudaStream_t s);
 // dq = dqacc (already scaled) cast to dtype with strides.
 cudaError_t launch_dq_convert(int dtype, const float* dqacc, void* dq, Strides st, int B, int H, int N,
                               cudaStream_t s);
