@@ -25,12 +25,15 @@
 // loops over the query tiles that see the key tile, for each query head of
 // the group, so dK and dV accumulate over the group in tensor memory.  The
 // steps of consecutive items form one global sequence: every ring and
-// barrier phase runs on the global step index, K/V are double-buffered so
-// the next item's K/V load overlaps the current item, and an item's dK, dV
-// leave tensor memory while the next item starts.
+// barrier phase runs on the global step index, K is double-buffered so the
+// next item's K load overlaps the current item (V, needed later in a step,
+// has one buffer, reloaded as soon as the last dP^T of an item has read it),
+// and an item's dK, dV leave tensor memory while the next item starts.
 //   * warp 16: TMA loads of K, V per item and of Q_i, dO_i (+ LSE_i, D_i
-//     rows) per step into a two-stage ring, and, three steps behind, the two
-//     TMA reduce-adds of each staged dQ_i into the float32 accumulator;
+//     rows) per step into a three-stage ring (the Q / dO loads are latency-
+//     bound: with two stages a step often waited for its tiles), and, three
+//     steps behind, the two TMA reduce-adds of each staged dQ_i into the
+//     float32 accumulator;
 //   * three MMA-issuing warps (one thread each): consecutive MMAs into the
 //     same accumulator complete about 126 cycles apart whatever their N, so
 //     each product is a latency chain, and independent chains are issued
@@ -62,14 +65,14 @@ namespace {
 
 constexpr int kThreads = 640;
 constexpr int kCompute = 512;   // threads of warps 0-15
-constexpr int NSB = 2;   // Q / dO stages
+constexpr int NSB = 3;   // Q / dO stages
 constexpr int NSTG = 1;  // float32 dQ staging buffers
 constexpr int kLag = 3;  // dQ reduce-adds trail the loads by this many steps
 
 struct BwdSmem {
   static constexpr int kK = 0;                      // 2 x 16 KB (double-buffered per item)
-  static constexpr int kV = 32768;                  // 2 x 16 KB
-  static constexpr int kQ = 65536;                  // NSB x 16 KB
+  static constexpr int kV = 32768;                  // 16 KB
+  static constexpr int kQ = 49152;                  // NSB x 16 KB
   static constexpr int kDO = kQ + NSB * 16384;      // NSB x 16 KB
   static constexpr int kDS = kDO + NSB * 16384;     // 32 KB: dS^T [2 chunks][128 keys][64 q]
   static constexpr int kDQ = kDS + 32768;           // NSTG x 32 KB: float32 dQ staging [buf][half][128][32]
@@ -77,13 +80,13 @@ struct BwdSmem {
   static constexpr int kInfo = kLD + NSB * 1024;    // (query tile, query head, batch) of the last kLag+1 steps
   static constexpr int kItem = kInfo + 64;          // the two published work items
   static constexpr int kBar = kItem + 64;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kBytes = kBar + 320;
   static constexpr int kDyn = kBytes + 1024;
 };
 
 struct BBars {
   uint64_t item_full[2], item_empty[2];   // the work-item hand-off from warp 16 to the other roles
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t k_full[2], k_empty[2], v_full, v_empty;
   uint64_t q_full[NSB], q_empty[NSB];
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free, dkv_full, pt_free;
   uint64_t dsm_free;
@@ -93,7 +96,7 @@ struct BBars {
   int abort;
 };
 
-static_assert(sizeof(BBars) <= 256, "barrier block overflows its shared-memory slot");
+static_assert(sizeof(BBars) <= 320, "barrier block overflows its shared-memory slot");
 static_assert(BwdSmem::kDyn <= 232448, "shared memory over the per-block limit");
 
 // One work item: key tile jt of K/V head hk of batch b, and its steps:
@@ -169,8 +172,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->item_full[s], 1);
       mbar_init(&bars->item_empty[s], 3 + kCompute);   // warps 17-19 and the compute threads
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 2);   // S/dP warp and dQ warp read K / V
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 2);    // S^T warp and dQ warp read K
     }
     for (int s = 0; s < NSB; ++s) {
       mbar_init(&bars->q_full[s], 1);
@@ -183,6 +186,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, kCompute);
     mbar_init(&bars->dkv_full, 1);
+    mbar_init(&bars->v_full, 1);
+    mbar_init(&bars->v_empty, 1);        // dP^T warp reads V
     mbar_init(&bars->pt_free, 1);
     mbar_init(&bars->dsm_free, 2);     // dK and dQ both read the shared dS^T tile
     for (int i = 0; i < 3; ++i) mbar_init(&bars->done[i], 1);
@@ -283,10 +288,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             continue;
           }
           const int kb = nkv & 1;
-          if (!(ok = mbar_wait(&bars->kv_empty[kb], ((uint32_t)(nkv >> 1) & 1u) ^ 1u, ctl))) break;
-          mbar_expect_tx(&bars->kv_full[kb], 32768);
-          tma_load_4d(smem + L::kK + kb * 16384, &tmK, &bars->kv_full[kb], 0, it.jt * kTile, it.hk, it.b);
-          tma_load_4d(smem + L::kV + kb * 16384, &tmV, &bars->kv_full[kb], 0, it.jt * kTile, it.hk, it.b);
+          if (!(ok = mbar_wait(&bars->k_empty[kb], ((uint32_t)(nkv >> 1) & 1u) ^ 1u, ctl))) break;
+          mbar_expect_tx(&bars->k_full[kb], 16384);
+          tma_load_4d(smem + L::kK + kb * 16384, &tmK, &bars->k_full[kb], 0, it.jt * kTile, it.hk, it.b);
+          const int vi = nkv;
           ++nkv;
           int qu = 0, hq = it.h0;
           for (int t = 0; t < it.steps && ok; ++t, ++g) {
@@ -300,6 +305,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             bulk_load(smem + L::kLD + st * 1024, a.lse2 + ld_row, 512, &bars->q_full[st]);
             bulk_load(smem + L::kLD + st * 1024 + 512, a.dvec + ld_row, 512, &bars->q_full[st]);
             info[g & 3] = make_int4(qi, hq, it.b, 0);
+            if (t == 0) {
+              // V has one buffer: it is reloaded once the previous item's last dP^T is done
+              if (!(ok = mbar_wait(&bars->v_empty, ((uint32_t)vi & 1u) ^ 1u, ctl))) break;
+              mbar_expect_tx(&bars->v_full, 16384);
+              tma_load_4d(smem + L::kV, &tmV, &bars->v_full, 0, it.jt * kTile, it.hk, it.b);
+            }
             if (++qu == it.n) { qu = 0; ++hq; }
             if (!(ok = reduce_to(g - kLag))) break;
           }
@@ -307,7 +318,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // the reduces still owed, then no copy may still be in flight
         if (ok) ok = reduce_to(g - 1);
         for (int t = max(0, g - NSB); t < g; ++t) mbar_wait(&bars->q_full[t % NSB], (uint32_t)(t / NSB) & 1u, ctl);
-        for (int t = max(0, nkv - 2); t < nkv; ++t) mbar_wait(&bars->kv_full[t & 1], (uint32_t)(t >> 1) & 1u, ctl);
+        for (int t = max(0, nkv - 2); t < nkv; ++t) mbar_wait(&bars->k_full[t & 1], (uint32_t)(t >> 1) & 1u, ctl);
+        if (nkv > 0) mbar_wait(&bars->v_full, (uint32_t)(nkv - 1) & 1u, ctl);
         bulk_wait_read0();
       }
     } else if (warp == 17) {
@@ -320,9 +332,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           const Item it = make_item(a, u);
           if (it.steps == 0) continue;
           const int kb = nkv & 1;
-          if (!(ok = mbar_wait(&bars->kv_full[kb], (uint32_t)(nkv >> 1) & 1u, ctl))) break;
+          if (!(ok = mbar_wait(&bars->k_full[kb], (uint32_t)(nkv >> 1) & 1u, ctl))) break;
+          const int vi = nkv;
           ++nkv;
-          const uint32_t sK = smem_u32(smem + L::kK + kb * 16384), sV = smem_u32(smem + L::kV + kb * 16384);
+          const uint32_t sK = smem_u32(smem + L::kK + kb * 16384), sV = smem_u32(smem + L::kV);
           for (int t = 0; t < it.steps && ok; ++t, ++g) {
             const int st = g % NSB;
             // S^T(g) = K Q_g^T once part 1 of step g-1 has read S^T(g-1)
@@ -336,6 +349,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mma_commit(&bars->s_full);
             // dP^T(g) = V dO_g^T once part 2 of step g-1 has read dP^T(g-1)
             if (g > 0 && !(ok = mbar_wait(&bars->ds_full, (uint32_t)(g - 1) & 1u, ctl))) break;
+            if (t == 0 && !(ok = mbar_wait(&bars->v_full, (uint32_t)vi & 1u, ctl))) break;
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -343,7 +357,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                      idST, k > 0 ? 1u : 0u);
             mma_commit(&bars->dp_full);
           }
-          mma_commit(&bars->kv_empty[kb]);   // this item's S^T and dP^T are done with K, V
+          mma_commit(&bars->k_empty[kb]);    // this item's S^T are done with K
+          mma_commit(&bars->v_empty);        // and its dP^T with V
         }
         mma_commit(&bars->done[0]);
         mbar_wait(&bars->done[0], 0, ctl);
@@ -411,7 +426,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mma_commit(&bars->dq_full);
             mma_commit(&bars->dsm_free);
           }
-          mma_commit(&bars->kv_empty[kb]);   // this item's dQ MMAs are done with K
+          mma_commit(&bars->k_empty[kb]);    // this item's dQ MMAs are done with K
         }
         mma_commit(&bars->done[2]);
         mbar_wait(&bars->done[2], 0, ctl);
