@@ -62,7 +62,7 @@ Layout layout(const fa_params* p, bool bwd) {
     const size_t rows = (size_t)p->B * p->H * L.npad;
     L.lse2 = take(rows * sizeof(float));
     L.dvec = take(rows * sizeof(float));
-    if (p->dtype != FA_DT_F32) L.dqacc = take((size_t)p->B * p->H * p->N * kHeadDim * sizeof(float));
+    if (p->dtype != FA_DT_F32) L.dqacc = take((size_t)p->B * p->H * p->N * p->d * sizeof(float));
     L.sched = take(sizeof(int));
   }
   L.total = off;
@@ -82,7 +82,8 @@ fa_status check_params(const fa_params* p) {
   if (p == nullptr) return FA_ERR_INVALID_ARG;
   if (p->B < 1 || p->H < 1 || p->N < 1 || p->d < 1) return FA_ERR_INVALID_ARG;
   if (p->dtype != FA_DT_F32 && p->dtype != FA_DT_F16 && p->dtype != FA_DT_BF16) return FA_ERR_INVALID_ARG;
-  if (p->d != kHeadDim) return FA_ERR_UNSUPPORTED;
+  // d = 64 on every path; d = 128 on the 16-bit tensor-core forward
+  if (p->d != 64 && !(p->d == 128 && p->dtype != FA_DT_F32)) return FA_ERR_UNSUPPORTED;
   if (p->stride_n < p->d || p->stride_h < 1 || p->stride_b < 1) return FA_ERR_INVALID_ARG;
   if (!(p->dropout_p >= 0.f && p->dropout_p < 1.f)) return FA_ERR_INVALID_ARG;
   if ((long long)p->B * p->H * p->N >= (1ll << 32)) return FA_ERR_UNSUPPORTED;
@@ -156,7 +157,7 @@ fa_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int
 fa_status map16(CUtensorMap* m, const void* base, const fa_params* p, int heads, Strides s) {
   const CUtensorMapDataType dt =
       p->dtype == FA_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return make_map(m, base, dt, 2, kHeadDim, kHeadDim, p, heads, s);
+  return make_map(m, base, dt, 2, p->d, 64, p, heads, s);   // 64-column (128-byte) boxes
 }
 
 MaskArgs mask_of(const fa_params* p, const Layout& L, uint8_t* ws) {
@@ -252,13 +253,14 @@ fa_status fa_fwd(const fa_params* p, const void* q, const void* k, const void* v
       (s = map16(&mv, v, p, hkv, skv)) != FA_OK || (s = map16(&mo, o, p, p->H, sd)) != FA_OK)
     return s;
   ProfScope prof(p, st);
-  return cuda_status(launch_fwd_tc(p->dtype, mq, mk, mv, mo, a, st));
+  return cuda_status(launch_fwd_tc(p->dtype, p->d, mq, mk, mv, mo, a, st));
 }
 
 fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v, const void* o, const void* dout,
                  const float* lse, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
   fa_status s = check_params(p);
   if (s != FA_OK) return s;
+  if (p->d != 64) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))

@@ -71,7 +71,8 @@ struct BwdArgs {
 // ---------------------------------------------------------------------------
 // Launchers (defined in the .cu files; all enqueue on `stream`).
 // ---------------------------------------------------------------------------
-cudaError_t launch_fwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+// d: head dimension, 64 or 128
+cudaError_t launch_fwd_tc(int dtype, int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& o, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s);

@@ -46,17 +46,23 @@ namespace {
 constexpr int kThreads = 384;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-constexpr int NS = 5;                       // K/V stages
-
+// Shared memory for head dimension D: the two query tiles, then rings of NS
+// K and NS V tiles.  A 128-row tile is D / 64 boxes of [128 rows][128 bytes]
+// (128-byte swizzle), 16 KB each.
+template <int D>
 struct FwdCfg {
-  static constexpr int kQ = 0;                           // 2 x 16 KB
-  static constexpr int kK = 32768;                       // NS x 16 KB
-  static constexpr int kV = kK + NS * 16384;             // NS x 16 KB
-  static constexpr int kBar = kV + NS * 16384;
+  static constexpr int kTB = 128 * D * 2;                // one tile
+  static constexpr int NS = D == 64 ? 5 : 2;             // K/V stages
+  static constexpr int kQ = 0;                           // 2 tiles
+  static constexpr int kK = 2 * kTB;                     // NS tiles
+  static constexpr int kV = kK + NS * kTB;               // NS tiles
+  static constexpr int kBar = kV + NS * kTB;
   static constexpr int kBytes = kBar + 512;
   static constexpr int kDyn = kBytes + 1024;             // + alignment slack
 };
+static_assert(FwdCfg<64>::kDyn <= 232448 && FwdCfg<128>::kDyn <= 232448, "shared memory over the per-block limit");
 
+template <int NS>
 struct Bars {
   uint64_t q_full;
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
@@ -119,7 +125,7 @@ struct StepPlan {
   __device__ __forceinline__ int load_of(int x) const { return x ? use[1] : use[0]; }
 };
 
-template <bool kWin>
+template <int NS, bool kWin>
 __device__ __forceinline__ StepPlan plan_step(const Slot (&sl)[2], int s, int& ld) {
   StepPlan p;
   p.nl = 0;
@@ -146,15 +152,23 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-template <typename T, bool kDrop, bool kWin>
+template <typename T, int D, bool kDrop, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
               const FwdArgs a) {
-  using C = FwdCfg;
+  using C = FwdCfg<D>;
+  constexpr int NS = C::NS;
+  constexpr int TB = C::kTB;
+  constexpr int NC = D / 64;                  // 64-column boxes per tile
+  // Tensor memory per slot (256 columns): S 128 | P 64 | O 64 for D = 64.
+  // For D = 128, O takes 128 columns and P (16 bit, packed two per column)
+  // overwrites the first 64 columns of S once the softmax has read S; the
+  // next S of the slot then waits for the PV MMA that reads P.
+  constexpr uint32_t kColP = D == 64 ? 128 : 0, kColO = D == 64 ? 192 : 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + C::kBar);
+  Bars<NS>* bars = reinterpret_cast<Bars<NS>*>(smem + C::kBar);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -213,17 +227,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      const uint32_t qbytes = (sl[0].n > 0 ? 16384u : 0u) + (sl[1].n > 0 ? 16384u : 0u);
+      const uint32_t qbytes = (sl[0].n > 0 ? (uint32_t)TB : 0u) + (sl[1].n > 0 ? (uint32_t)TB : 0u);
       if (qbytes > 0) {
         mbar_expect_tx(&bars->q_full, qbytes);
 #pragma unroll
         for (int x = 0; x < 2; ++x)
-          if (sl[x].n > 0) tma_load_4d(smem + C::kQ + x * 16384, &tmQ, &bars->q_full, 0, sl[x].qt * kTile, h, b);
+          if (sl[x].n > 0)
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+              tma_load_4d(smem + C::kQ + x * TB + c * 16384, &tmQ, &bars->q_full, c * 64, sl[x].qt * kTile, h, b);
       }
       int ld = 0;
       bool ok = true;
       for (int s = 0; s < smax && ok; ++s) {
-        const StepPlan p = plan_step<kWin>(sl, s, ld);
+        const StepPlan p = plan_step<NS, kWin>(sl, s, ld);
 #pragma unroll
         for (int l = 0; l < 2; ++l) {
           if (l >= p.nl) break;
@@ -231,10 +248,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           if (!(ok = mbar_wait(&bars->k_empty[st], p.ph[l] ^ 1u, ctl) &&
                      mbar_wait(&bars->v_empty[st], p.ph[l] ^ 1u, ctl)))
             break;
-          mbar_expect_tx(&bars->k_full[st], 16384);
-          tma_load_4d(smem + C::kK + st * 16384, &tmK, &bars->k_full[st], 0, p.kv[l] * kTile, hk, b);
-          mbar_expect_tx(&bars->v_full[st], 16384);
-          tma_load_4d(smem + C::kV + st * 16384, &tmV, &bars->v_full[st], 0, p.kv[l] * kTile, hk, b);
+          mbar_expect_tx(&bars->k_full[st], TB);
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            tma_load_4d(smem + C::kK + st * TB + c * 16384, &tmK, &bars->k_full[st], c * 64, p.kv[l] * kTile, hk, b);
+          mbar_expect_tx(&bars->v_full[st], TB);
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            tma_load_4d(smem + C::kV + st * TB + c * 16384, &tmV, &bars->v_full[st], c * 64, p.kv[l] * kTile, hk, b);
         }
       }
       // Before leaving, make sure no load is still writing shared memory.
@@ -249,23 +270,30 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (lane == 0 && smax > 0) {
       constexpr uint32_t idS = idesc_f16(128, 128, ab, 0, 0);
       const uint64_t qd[2] = {sdesc_sw128(smem_u32(smem + C::kQ), 16, 1024),
-                              sdesc_sw128(smem_u32(smem + C::kQ + 16384), 16, 1024)};
+                              sdesc_sw128(smem_u32(smem + C::kQ + TB), 16, 1024)};
       const uint64_t kd0 = sdesc_sw128(smem_u32(smem + C::kK), 16, 1024);
       bool ok = mbar_wait(&bars->q_full, 0, ctl);
       int ld = 0;
       for (int s = 0; s < smax && ok; ++s) {
-        const StepPlan p = plan_step<kWin>(sl, s, ld);
+        const StepPlan p = plan_step<NS, kWin>(sl, s, ld);
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           if (!ok || s >= sl[x].n) continue;
           const int l = p.use[x];
-          if (s > 0 && !(ok = mbar_wait(&bars->s_free[x], (uint32_t)(s - 1) & 1u, ctl))) break;
+          // S_x(s) overwrites S_x(s-1) (D = 64: once the softmax has read it)
+          // or P_x(s-1) (D = 128: once PV_x(s-1) has read it)
+          if (s > 0 && !(ok = mbar_wait(D == 64 ? &bars->s_free[x] : &bars->pv_done[x], (uint32_t)(s - 1) & 1u, ctl)))
+            break;
           if (!(ok = mbar_wait(&bars->k_full[p.stage(l)], p.parity(l), ctl))) break;
           tc_fence_after();
-          const uint64_t kd = kd0 + (uint64_t)((p.stage(l) * 16384) >> 4);
+          const uint64_t kd = kd0 + (uint64_t)((p.stage(l) * TB) >> 4);
           const uint32_t tS = tmem + x * 256;
+          // K-dim = D in steps of 16: box k / 4, 32 bytes per step within it
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mma_ss(tS, qd[x] + 2 * k, kd + 2 * k, idS, k > 0 ? 1u : 0u);
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t o = (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+            mma_ss(tS, qd[x] + o, kd + o, idS, k > 0 ? 1u : 0u);
+          }
           mma_commit(&bars->s_full[x]);
         }
 #pragma unroll
@@ -279,14 +307,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // ===================== PV issuer of slot x =====================
     const int x = warp - 10;
     if (lane == 0 && smax > 0) {
-      constexpr uint32_t idPV = idesc_f16(128, 64, ab, 0, 1);
+      constexpr uint32_t idPV = idesc_f16(128, D, ab, 0, 1);
       const uint64_t vd0 = sdesc_sw128(smem_u32(smem + C::kV), 16384, 1024);
-      const uint32_t tP = tmem + x * 256 + 128, tO = tmem + x * 256 + 192;
+      const uint32_t tP = tmem + x * 256 + kColP, tO = tmem + x * 256 + kColO;
       const int n = x ? sl[1].n : sl[0].n;
       int ld = 0;
       bool ok = true;
       for (int s = 0; s < smax && ok; ++s) {
-        const StepPlan p = plan_step<kWin>(sl, s, ld);
+        const StepPlan p = plan_step<NS, kWin>(sl, s, ld);
         const int mine = p.load_of(x);
         if (s < n) {
           const int st = p.stage(mine);
@@ -294,7 +322,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                      mbar_wait(&bars->v_full[st], p.parity(mine), ctl)))
             break;
           tc_fence_after();
-          const uint64_t vd = vd0 + (uint64_t)((st * 16384) >> 4);
+          const uint64_t vd = vd0 + (uint64_t)((st * TB) >> 4);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             mma_ts(tO, tP + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idPV, (s > 0 || k > 0) ? 1u : 0u);
@@ -326,7 +354,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const Slot S = x ? sl[1] : sl[0];
     const int i = S.qt * kTile + r;             // global query row
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tmem + x * 256 + lane_off, tP = tS + 128, tO = tS + 192;
+    const uint32_t tS = tmem + x * 256 + lane_off, tP = tS + kColP, tO = tS + kColO;
     const float sl2 = a.scale_log2;
     const int jmax = a.mask.causal ? min(Lk - 1, i) : (Lk - 1);
     const int jmin = kWin ? i - a.mask.window + 1 : 0;   // first key of the sliding window
@@ -346,7 +374,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) reg_fence32(sr[cc]);
       tc_fence_before();
-      mbar_arrive(&bars->s_free[x]);             // S_x(s+1) may now overwrite the S columns
+      if constexpr (D == 64) mbar_arrive(&bars->s_free[x]);   // S_x(s+1) may now overwrite the S columns
 
       // mask (only boundary tiles) and row max of the raw scores
       const int jl = jmax - kv * kTile;
@@ -430,7 +458,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       // any of its rows needs it (alpha is exactly 1 for the other rows)
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = 0; hf < D / 32; ++hf) {
           uint32_t o[32];
           tmem_ld32(tO + hf * 32, o);
           tmem_wait_ld();
@@ -447,53 +475,54 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
     // ---- epilogue: O / l -> 16 bit -> shared -> TMA store; logsumexp
     if (!named_bar_or(1 + x, 128, !ok || bars->abort)) {
-      float o[64];
-      if (S.n > 0) {
-        if (warp_wait(&bars->pv_done[x], (uint32_t)(S.n - 1) & 1u, ctl)) {
-          tc_fence_after();
+      // the last PV of the slot (warp-uniform: warp_wait agrees across the warp)
+      const bool have = S.n > 0 && warp_wait(&bars->pv_done[x], (uint32_t)(S.n - 1) & 1u, ctl);
+      if (have) tc_fence_after();
+      const float inv = l_rnd > 0.f ? 1.f / l_rnd : 0.f;
+      const bool row_ok = i < a.N && S.qt < a.nq;
+      const size_t row = (size_t)(b * a.H + h) * a.N + i;
+      uint8_t* ob = smem + C::kQ + x * TB;      // Q_x is dead once O_x is final
+      // 64 columns at a time: tensor memory -> O / l -> 16 bit -> swizzled box hh
+#pragma unroll 1
+      for (int hh = 0; hh < NC; ++hh) {
+        float o[64];
+        if (have) {
           uint32_t raw[2][32];
-          tmem_ld32(tO, raw[0]);
-          tmem_ld32(tO + 32, raw[1]);
+          tmem_ld32(tO + hh * 64, raw[0]);
+          tmem_ld32(tO + hh * 64 + 32, raw[1]);
           tmem_wait_ld();
           reg_fence32(raw[0]);
           reg_fence32(raw[1]);
-          const float inv = l_rnd > 0.f ? 1.f / l_rnd : 0.f;
 #pragma unroll
           for (int c = 0; c < 64; ++c) o[c] = __uint_as_float(raw[c >> 5][c & 31]) * inv;
         } else {
 #pragma unroll
           for (int c = 0; c < 64; ++c) o[c] = 0.f;
         }
-      } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) o[c] = 0.f;
-      }
-      uint8_t* ob = smem + C::kQ + x * 16384;   // Q_x is dead once O_x is final
+        for (int j = 0; j < 8; ++j) {
+          uint32_t w[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t w[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) w[t] = Cvt<T>::pack(o[j * 8 + 2 * t], o[j * 8 + 2 * t + 1]);
-        const uint32_t off = r * 128 + (((j ^ r) & 7) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                     :: "r"(smem_u32(ob + off)), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1 + x, 128);
-      if (r == 0 && S.qt < a.nq) {
-        tma_store_4d(&tmO, ob, 0, S.qt * kTile, h, b);
-        bulk_commit();
-        bulk_wait_read0();
-      }
-      if (i < a.N && S.qt < a.nq) {
-        const size_t row = (size_t)(b * a.H + h) * a.N + i;
-        a.lse[row] = l_true > 0.f ? (m_run + lg2(l_true)) * kLn2 : -INFINITY;
-        if (a.o_f32 != nullptr) {
-          float4* dst = reinterpret_cast<float4*>(a.o_f32 + row * 64);
+          for (int t = 0; t < 4; ++t) w[t] = Cvt<T>::pack(o[j * 8 + 2 * t], o[j * 8 + 2 * t + 1]);
+          const uint32_t off = hh * 16384 + r * 128 + (((j ^ r) & 7) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                       :: "r"(smem_u32(ob + off)), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
+        }
+        if (row_ok && a.o_f32 != nullptr) {
+          float4* dst = reinterpret_cast<float4*>(a.o_f32 + row * D + hh * 64);
 #pragma unroll
           for (int c = 0; c < 16; ++c) dst[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
         }
       }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + x, 128);
+      if (r == 0 && S.qt < a.nq) {
+#pragma unroll
+        for (int hh = 0; hh < NC; ++hh) tma_store_4d(&tmO, ob + hh * 16384, hh * 64, S.qt * kTile, h, b);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+      if (row_ok) a.lse[row] = l_true > 0.f ? (m_run + lg2(l_true)) * kLn2 : -INFINITY;
     }
   }
 
@@ -505,38 +534,37 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
 }
 
-template <typename T, bool kDrop, bool kWin>
+template <typename T, int D, bool kDrop, bool kWin>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
                      const FwdArgs& a, cudaStream_t s) {
-  auto kern = fwd_tc_kernel<T, kDrop, kWin>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg::kDyn);
+  auto kern = fwd_tc_kernel<T, D, kDrop, kWin>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kDyn);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(a.npairs * a.B * a.H);
   if (grid == 0) return cudaSuccess;
-  kern<<<grid, kThreads, FwdCfg::kDyn, s>>>(q, k, v, o, a);
+  kern<<<grid, kThreads, FwdCfg<D>::kDyn, s>>>(q, k, v, o, a);
   return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_d(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                     const FwdArgs& a, cudaStream_t s) {
+  const int sel = (a.drop.enabled ? 1 : 0) | (a.mask.window > 0 ? 2 : 0);
+  switch (sel) {
+    case 0: return launch_t<T, D, false, false>(q, k, v, o, a, s);
+    case 1: return launch_t<T, D, true, false>(q, k, v, o, a, s);
+    case 2: return launch_t<T, D, false, true>(q, k, v, o, a, s);
+    default: return launch_t<T, D, true, true>(q, k, v, o, a, s);
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_fwd_tc(int dtype, int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& o, const FwdArgs& a, cudaStream_t s) {
-  const int sel = (a.drop.enabled ? 1 : 0) | (a.mask.window > 0 ? 2 : 0);
-  if (dtype == FA_DT_BF16) {
-    using B = __nv_bfloat16;
-    switch (sel) {
-      case 0: return launch_t<B, false, false>(q, k, v, o, a, s);
-      case 1: return launch_t<B, true, false>(q, k, v, o, a, s);
-      case 2: return launch_t<B, false, true>(q, k, v, o, a, s);
-      default: return launch_t<B, true, true>(q, k, v, o, a, s);
-    }
-  }
-  switch (sel) {
-    case 0: return launch_t<__half, false, false>(q, k, v, o, a, s);
-    case 1: return launch_t<__half, true, false>(q, k, v, o, a, s);
-    case 2: return launch_t<__half, false, true>(q, k, v, o, a, s);
-    default: return launch_t<__half, true, true>(q, k, v, o, a, s);
-  }
+  if (dtype == FA_DT_BF16)
+    return d == 128 ? launch_d<__nv_bfloat16, 128>(q, k, v, o, a, s) : launch_d<__nv_bfloat16, 64>(q, k, v, o, a, s);
+  return d == 128 ? launch_d<__half, 128>(q, k, v, o, a, s) : launch_d<__half, 64>(q, k, v, o, a, s);
 }
 
 }  // namespace fa

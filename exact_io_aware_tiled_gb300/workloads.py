@@ -123,4 +123,10 @@ CONFIGS = {
     # N = 8192 with a window of 512 keys
     "window512_8k": Workload("window512_8k", B=4, H=16, N=8192, dtype="bf16", causal=True,
                              window=512, seed=20267),
+    # head dimension 128 at the GPT-2-medium model width (8 heads x 128 =
+    # 16 x 64), the case the pages single out as the one where the on-chip
+    # tile budget gets tight (marketmaker.cc, "O que isso custou"; lynx-cortex,
+    # "Lo que Flash forward no hace"); same FLOPs as the d = 64 workload
+    "gpt2_medium_d128_causal": Workload("gpt2_medium_d128_causal", B=64, H=8, N=1024, d=128,
+                                        dtype="bf16", causal=True, seed=20268),
 }

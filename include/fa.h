@@ -36,6 +36,11 @@
  *     window = w > 0 and causal set, key j is visible to query i iff
  *     i - w < j <= i; whole K/V tiles outside every window of a query tile
  *     are skipped.
+ *   - Head dimension: d = 64 for every dtype; d = 128 for float16 and
+ *     bfloat16 in fa_fwd (the pages name d = 128 as the case where the
+ *     on-chip tile budget gets tight: marketmaker.cc, "O que isso custou";
+ *     lynx-cortex, "Lo que Flash forward no hace").  fa_bwd with d = 128
+ *     returns FA_ERR_UNSUPPORTED.
  *   - Ownership: the caller owns every buffer and the stream.  The library
  *     never allocates, frees or synchronises device memory, except that
  *     fa_check_status synchronises the stream it is given.  Work is enqueued
@@ -74,7 +79,7 @@ typedef enum {
 typedef enum { FA_DT_F32 = 0, FA_DT_F16 = 1, FA_DT_BF16 = 2 } fa_dtype;
 
 typedef struct {
-  int32_t B, H, N, d;        /* batch, heads, sequence length, head dim (64)    */
+  int32_t B, H, N, d;        /* batch, heads, sequence length, head dim         */
   int32_t dtype;             /* fa_dtype of Q,K,V,O,dO,dQ,dK,dV                 */
   int64_t stride_b;          /* element strides shared by all [B,H,N,d] tensors */
   int64_t stride_h;

@@ -96,7 +96,8 @@ FAKE = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: validation fail
 
 
 @pytest.mark.parametrize("mut,code", [
-    (dict(d=128), 2),                 # head dim 128 not built yet -> UNSUPPORTED
+    (dict(d=96), 2),                  # only head dims 64 and 128 are built
+    (dict(d=128, dtype=0), 2),        # d = 128 has no float32 path
     (dict(d=0), 1),
     (dict(N=0), 1),
     (dict(dtype=7), 1),
@@ -129,6 +130,9 @@ def test_null_and_misaligned_pointers_and_small_workspace(lib):
     assert lib.fa_bwd(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, ws, 1 << 30,
                       None) == 1
     assert lib.fa_bwd(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, 16, None) == 4
+    p128 = _params(d=128, stride_n=128, stride_h=200 * 128, stride_b=3 * 200 * 128)
+    assert lib.fa_bwd(ctypes.byref(p128), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, 1 << 30,
+                      None) == 2
     assert lib.fa_dropout_mask(ctypes.byref(p), 2, 0, 0, 1, FAKE, None) == 1      # b out of range
     assert lib.fa_dropout_mask(ctypes.byref(p), 0, 0, 190, 20, FAKE, None) == 1   # rows past N
 

@@ -106,9 +106,12 @@ def test_repeated_calls_are_deterministic_in_forward():
 
 
 def test_host_errors_are_raised_not_hidden():
-    q = torch.zeros((1, 1, 64, 128), device="cuda", dtype=torch.bfloat16)
+    q = torch.zeros((1, 1, 64, 96), device="cuda", dtype=torch.bfloat16)   # head dim 96 is not built
     with pytest.raises(fa.FAError):
         fa.fwd(q, q, q)
+    q32 = torch.zeros((1, 1, 64, 128), device="cuda", dtype=torch.float32)  # d = 128 has no float32 path
+    with pytest.raises(fa.FAError):
+        fa.fwd(q32, q32, q32)
 
 
 # ---- grouped-query attention (living-dl-book, efficient attention, section 6)
