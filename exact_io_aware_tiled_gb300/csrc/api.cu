@@ -139,14 +139,14 @@ DropoutArgs dropout_of(const fa_params* p) {
   return d;
 }
 
-// 4-D map over a [B,heads,N,cols] tensor: dims (cols, N, heads, B), box (box_c, 128, 1, 1), 128-byte swizzle.
+// 4-D map over a [B,heads,N,cols] tensor: dims (cols, N, heads, B), box (box_c, box_r, 1, 1), 128-byte swizzle.
 fa_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int cols, int box_c,
-                   const fa_params* p, int heads, Strides s) {
+                   const fa_params* p, int heads, Strides s, int box_r = kTile) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return FA_ERR_CUDA;
   cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)p->N, (cuuint64_t)heads, (cuuint64_t)p->B};
   cuuint64_t strides[3] = {(cuuint64_t)(s.n * esize), (cuuint64_t)(s.h * esize), (cuuint64_t)(s.b * esize)};
-  cuuint32_t box[4] = {(cuuint32_t)box_c, (cuuint32_t)kTile, 1, 1};
+  cuuint32_t box[4] = {(cuuint32_t)box_c, (cuuint32_t)box_r, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -154,10 +154,10 @@ fa_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status map16(CUtensorMap* m, const void* base, const fa_params* p, int heads, Strides s) {
+fa_status map16(CUtensorMap* m, const void* base, const fa_params* p, int heads, Strides s, int rows = kTile) {
   const CUtensorMapDataType dt =
       p->dtype == FA_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return make_map(m, base, dt, 2, p->d, 64, p, heads, s);   // 64-column (128-byte) boxes
+  return make_map(m, base, dt, 2, p->d, 64, p, heads, s, rows);   // 64-column (128-byte) boxes
 }
 
 MaskArgs mask_of(const fa_params* p, const Layout& L, uint8_t* ws) {
@@ -260,7 +260,6 @@ fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v
                  const float* lse, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
   fa_status s = check_params(p);
   if (s != FA_OK) return s;
-  if (p->d != 64) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -289,7 +288,7 @@ fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v
   if ((s = prepare_common(p, L, w, st)) != FA_OK) return s;
   float* dqacc = p->dtype == FA_DT_F32 ? nullptr : reinterpret_cast<float*>(w + L.dqacc);
   a.sched = reinterpret_cast<int*>(w + L.sched);
-  cudaError_t e = launch_bwd_prep(p->dtype, o, dout, sd, lse, p->B, p->H, p->N, L.npad,
+  cudaError_t e = launch_bwd_prep(p->dtype, o, dout, sd, lse, p->B, p->H, p->N, L.npad, p->d,
                                   reinterpret_cast<float*>(w + L.lse2), reinterpret_cast<float*>(w + L.dvec), dqacc,
                                   a.sched, st);
   if (e != cudaSuccess) return FA_ERR_CUDA;
@@ -298,20 +297,25 @@ fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v
     return cuda_status(launch_bwd_simt((const float*)q, (const float*)k, (const float*)v, (const float*)dout,
                                        (float*)dq, (float*)dk, (float*)dv, sd, skv, a, st));
   }
+  // d = 64: 128-row query steps; d = 128: 64-row query steps (Q, dO and the
+  // float32 dQ accumulator are moved in 64-row boxes)
   CUtensorMap mq, mk, mv, mdo, macc;
-  Strides acc_st{(int64_t)p->H * p->N * kHeadDim, (int64_t)p->N * kHeadDim, kHeadDim};
-  if ((s = map16(&mq, q, p, p->H, sd)) != FA_OK || (s = map16(&mk, k, p, hkv, skv)) != FA_OK ||
-      (s = map16(&mv, v, p, hkv, skv)) != FA_OK || (s = map16(&mdo, dout, p, p->H, sd)) != FA_OK ||
-      (s = make_map(&macc, dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kHeadDim, 32, p, p->H, acc_st)) != FA_OK)
+  const int qrows = p->d == 128 ? 64 : kTile;
+  Strides acc_st{(int64_t)p->H * p->N * p->d, (int64_t)p->N * p->d, p->d};
+  if ((s = map16(&mq, q, p, p->H, sd, qrows)) != FA_OK || (s = map16(&mk, k, p, hkv, skv)) != FA_OK ||
+      (s = map16(&mv, v, p, hkv, skv)) != FA_OK || (s = map16(&mdo, dout, p, p->H, sd, qrows)) != FA_OK ||
+      (s = make_map(&macc, dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->d, 32, p, p->H, acc_st, qrows)) != FA_OK)
     return s;
   a.dk = dk;
   a.dv = dv;
   a.kst = skv;
   {
     ProfScope prof(p, st);
-    if ((e = launch_bwd_tc(p->dtype, mq, mk, mv, mdo, macc, a, st)) != cudaSuccess) return FA_ERR_CUDA;
+    e = p->d == 128 ? launch_bwd_tc128(p->dtype, mq, mk, mv, mdo, macc, a, st)
+                    : launch_bwd_tc(p->dtype, mq, mk, mv, mdo, macc, a, st);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
   }
-  return cuda_status(launch_dq_convert(p->dtype, dqacc, dq, sd, p->B, p->H, p->N, st));
+  return cuda_status(launch_dq_convert(p->dtype, dqacc, dq, sd, p->B, p->H, p->N, p->d, st));
 }
 
 fa_status fa_check_status(const void* ws, void* stream) {

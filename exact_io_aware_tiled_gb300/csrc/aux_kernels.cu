@@ -40,12 +40,13 @@ template <typename T> struct Vec8 {
   }
 };
 
-// It also clears the float32 dQ accumulator row (when there is one): the
-// same threads write the row's 64 zeros, 32 bytes each, so the clearing
-// rides on this pass instead of a separate memset.
+// Head dimension d (64 or 128): thread `part` of a row takes columns
+// part*8 + 64m.  It also clears the float32 dQ accumulator row (when there is
+// one): the same threads write the row's d zeros, 32 bytes per 8 columns, so
+// the clearing rides on this pass instead of a separate memset.
 template <typename T>
 __global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ dout, Strides st,
-                                const float* __restrict__ lse, int B, int H, int N, int npad,
+                                const float* __restrict__ lse, int B, int H, int N, int npad, int dh,
                                 float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dqacc,
                                 int* __restrict__ sched) {
   if (sched != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;   // backward work counter
@@ -58,12 +59,14 @@ __global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ d
   float d = 0.f;
   if (live && i < N) {
     const int b = bh / H, h = bh % H;
-    const size_t off = (size_t)b * st.b + (size_t)h * st.h + (size_t)i * st.n + part * 8;
-    d = Vec8<T>::dot(o + off, dout + off);
-    if (dqacc != nullptr) {
-      float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * N + i) * 64 + part * 8);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const size_t off = (size_t)b * st.b + (size_t)h * st.h + (size_t)i * st.n;
+    for (int c = part * 8; c < dh; c += 64) {
+      d += Vec8<T>::dot(o + off + c, dout + off + c);
+      if (dqacc != nullptr) {
+        float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * N + i) * dh + c);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
   d += __shfl_xor_sync(0xffffffffu, d, 1);
@@ -82,12 +85,12 @@ __global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ d
 
 template <typename T>
 __global__ void dq_convert_kernel(const float* __restrict__ acc, T* __restrict__ dq, Strides st, int H, int N,
-                                  long long nrows) {
-  // 8 consecutive elements per thread
+                                  int dh, long long nrows) {
+  // 8 consecutive elements per thread; rows of dh (64 or 128) columns
   const long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8;
-  if (e >= nrows * 64) return;
-  const long long row = e / 64;
-  const int c = (int)(e % 64);
+  if (e >= nrows * dh) return;
+  const long long row = e / dh;
+  const int c = (int)(e % dh);
   const int bh = (int)(row / N), i = (int)(row % N);
   const int b = bh / H, h = bh % H;
   const float4 x0 = *reinterpret_cast<const float4*>(acc + e);
@@ -151,33 +154,34 @@ __global__ void dropout_mask_kernel(DropoutArgs d, int H, int N, int b, int h, i
 }  // namespace
 
 cudaError_t launch_bwd_prep(int dtype, const void* o, const void* dout, Strides st, const float* lse, int B, int H,
-                            int N, int npad, float* lse2, float* dvec, float* dqacc, int* sched, cudaStream_t s) {
+                            int N, int npad, int d, float* lse2, float* dvec, float* dqacc, int* sched,
+                            cudaStream_t s) {
   const long long rows = (long long)B * H * npad;
   const int threads = 256;
   const long long blocks = (rows * 8 + threads - 1) / threads;
   if (dtype == FA_DT_BF16)
     bwd_prep_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, s>>>(
-        (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, st, lse, B, H, N, npad, lse2, dvec, dqacc, sched);
+        (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, st, lse, B, H, N, npad, d, lse2, dvec, dqacc, sched);
   else if (dtype == FA_DT_F16)
     bwd_prep_kernel<__half><<<(unsigned)blocks, threads, 0, s>>>((const __half*)o, (const __half*)dout, st, lse, B,
-                                                                 H, N, npad, lse2, dvec, dqacc, sched);
+                                                                 H, N, npad, d, lse2, dvec, dqacc, sched);
   else
     bwd_prep_kernel<float><<<(unsigned)blocks, threads, 0, s>>>((const float*)o, (const float*)dout, st, lse, B, H,
-                                                                N, npad, lse2, dvec, dqacc, sched);
+                                                                N, npad, d, lse2, dvec, dqacc, sched);
   return cudaGetLastError();
 }
 
-cudaError_t launch_dq_convert(int dtype, const float* dqacc, void* dq, Strides st, int B, int H, int N,
+cudaError_t launch_dq_convert(int dtype, const float* dqacc, void* dq, Strides st, int B, int H, int N, int d,
                               cudaStream_t s) {
   const long long nrows = (long long)B * H * N;
-  const long long threads_total = nrows * 8;
+  const long long threads_total = nrows * d / 8;
   const int threads = 256;
   const unsigned blocks = (unsigned)((threads_total + threads - 1) / threads);
   if (blocks == 0) return cudaSuccess;
   if (dtype == FA_DT_BF16)
-    dq_convert_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(dqacc, (__nv_bfloat16*)dq, st, H, N, nrows);
+    dq_convert_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(dqacc, (__nv_bfloat16*)dq, st, H, N, d, nrows);
   else
-    dq_convert_kernel<__half><<<blocks, threads, 0, s>>>(dqacc, (__half*)dq, st, H, N, nrows);
+    dq_convert_kernel<__half><<<blocks, threads, 0, s>>>(dqacc, (__half*)dq, st, H, N, d, nrows);
   return cudaGetLastError();
 }
 

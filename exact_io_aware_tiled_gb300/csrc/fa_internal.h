@@ -13,7 +13,6 @@ namespace fa {
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
 constexpr int kTile = 128;       // query rows (and key rows) per tile
-constexpr int kHeadDim = 64;     // head dimension handled by the kernels
 
 struct Strides { int64_t b, h, n; };
 
@@ -76,6 +75,9 @@ cudaError_t launch_fwd_tc(int dtype, int d, const CUtensorMap& q, const CUtensor
                           const CUtensorMap& o, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s);
+// Head dimension 128 (Q, dO and the dQ accumulator maps have 64-row boxes).
+cudaError_t launch_bwd_tc128(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                             const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s);
 
 // st: strides of Q, O, dO, dQ ([B,H,N,d]); kst: strides of K, V, dK, dV ([B,H_kv,N,d]).
 cudaError_t launch_fwd_simt(const float* q, const float* k, const float* v, float* o, Strides st,
@@ -86,10 +88,10 @@ cudaError_t launch_bwd_simt(const float* q, const float* k, const float* v, cons
 
 // D = rowsum(dO o O) and the padded LSE*log2e / D arrays; the same pass clears dqacc if given.
 cudaError_t launch_bwd_prep(int dtype, const void* o, const void* dout, Strides st, const float* lse,
-                            int B, int H, int N, int npad, float* lse2, float* dvec, float* dqacc,
+                            int B, int H, int N, int npad, int d, float* lse2, float* dvec, float* dqacc,
                             int* sched, cudaStream_t s);
 // dq = dqacc (already scaled) cast to dtype with strides.
-cudaError_t launch_dq_convert(int dtype, const float* dqacc, void* dq, Strides st, int B, int H, int N,
+cudaError_t launch_dq_convert(int dtype, const float* dqacc, void* dq, Strides st, int B, int H, int N, int d,
                               cudaStream_t s);
 // Row / column block lists of a dense [nb][nb] uint8 block mask.
 cudaError_t launch_block_lists(const uint8_t* mask, int nb, int16_t* row_list, int32_t* row_cnt,

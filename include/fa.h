@@ -37,10 +37,10 @@
  *     i - w < j <= i; whole K/V tiles outside every window of a query tile
  *     are skipped.
  *   - Head dimension: d = 64 for every dtype; d = 128 for float16 and
- *     bfloat16 in fa_fwd (the pages name d = 128 as the case where the
- *     on-chip tile budget gets tight: marketmaker.cc, "O que isso custou";
- *     lynx-cortex, "Lo que Flash forward no hace").  fa_bwd with d = 128
- *     returns FA_ERR_UNSUPPORTED.
+ *     bfloat16 (the pages name d = 128 as the case where the on-chip tile
+ *     budget gets tight: marketmaker.cc, "O que isso custou"; lynx-cortex,
+ *     "Lo que Flash forward no hace").  Other values, and d = 128 with
+ *     float32, return FA_ERR_UNSUPPORTED.
  *   - Ownership: the caller owns every buffer and the stream.  The library
  *     never allocates, frees or synchronises device memory, except that
  *     fa_check_status synchronises the stream it is given.  Work is enqueued

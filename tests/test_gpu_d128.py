@@ -1,6 +1,7 @@
 """GPU parity at head dimension 128: the forward kernel (P overwrites S in
-tensor memory, two 64-column boxes per tile) against the float64 oracle on
-whole heads, over ragged tails and every mask, and on sampled rows of the
+tensor memory, two 64-column boxes per tile) and the backward kernel (64-row
+query steps, dQ formed transposed) against the float64 oracle on whole
+heads, over ragged tails and every mask, and on sampled rows of the
 GPT-2-medium-width workload with 8 heads of 128."""
 import numpy as np
 import pytest
@@ -24,7 +25,7 @@ def _wl(N, dtype="bf16", B=2, H=3, seed=11, **kw):
 
 
 def _check_all_heads(wl, inp=None, layout="bhnd"):
-    inp = W.make_inputs(wl, grads=False) if inp is None else inp
+    inp = W.make_inputs(wl) if inp is None else inp
     got = run_gpu(wl, inp, layout=layout)
     for b in range(wl.B):
         for h in range(wl.H):
@@ -64,7 +65,7 @@ def test_rescale_decided_per_row_within_a_warp():
     # (see the d = 64 test of the same name); at d = 128 the rescale spans
     # four 32-column chunks of O
     wl = _wl(256, "bf16", B=1, H=2, seed=13)
-    inp = W.make_inputs(wl, grads=False)
+    inp = W.make_inputs(wl)
     qs = torch.where(torch.arange(256) % 2 == 0, 4.0, 0.1).view(1, 1, 256, 1)
     ks = torch.where(torch.arange(256) < 128, 0.1, 4.0).view(1, 1, 256, 1)
     inp["q"] = (inp["q"].float() * qs).to(torch.bfloat16)
@@ -73,19 +74,24 @@ def test_rescale_decided_per_row_within_a_warp():
         _check_all_heads(w, inp)
 
 
-def test_backward_is_refused_not_faked():
-    wl = _wl(256, "bf16", B=1, H=1)
-    inp = {k: v.cuda() for k, v in W.make_inputs(wl).items()}
-    o, lse = fa.fwd(inp["q"], inp["k"], inp["v"])[:2]
-    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
-        fa.bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse)
-
-
 def test_gpt2_medium_d128_causal_sampled():
     wl = W.CONFIGS["gpt2_medium_d128_causal"]
-    inp = W.make_inputs(wl, grads=False)
+    inp = W.make_inputs(wl)
     got = run_gpu(wl, inp)
     for b, h in [(0, 0), (63, 7)]:
         check_head(wl, inp, got, b, h)
     rows = sample_rows(wl.N, seed=128, extra=64)
-    check_head(wl, inp, got, 31, 3, rows=rows)
+    check_head(wl, inp, got, 31, 3, rows=rows, cols=rows)
+
+
+@pytest.mark.parametrize("p", [0.1, 0.5])
+def test_dropout(p):
+    _check_all_heads(_wl(257, "f16", B=1, H=2, dropout_p=p))
+
+
+def test_empty_key_tiles_and_ragged_half_steps():
+    # keys past L_b leave whole 128-key items empty (dK = dV = 0 written
+    # without a step), and N = 129 makes the last 128-row query tile's second
+    # 64-row half start past N
+    _check_all_heads(_wl(129 + 256, "bf16", B=3, H=2, seqlens=np.array([1, 129, 385], dtype=np.int32)))
+    _check_all_heads(_wl(129, "bf16", B=1, H=2, causal=True))
