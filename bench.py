@@ -403,7 +403,8 @@ def _source_hash(which):
     import hashlib
     m = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_io_aware_tiled_gb300", "csrc")
-    for f in ("%s_tc.cu" % which, "common.cuh"):
+    files = ["%s_tc.cu" % which, "common.cuh"] + (["bwd_items.cuh"] if which == "bwd" else [])
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             m.update(fh.read())
     return m.hexdigest()[:16]
