@@ -20,7 +20,16 @@ block-sparse paragraph):
 * block-sparse: kept(I, J) iff I == J or I ^ J is a power of two over
   N / 128 blocks;
 * grouped-query: K and V are drawn with ``H_kv`` heads ([B, H_kv, N, d]);
-* the sliding window is a mask parameter (``window``) and draws nothing.
+* the sliding window is a mask parameter (``window``) and draws nothing;
+* outliers (FP8 error study): with ``outlier_rate`` > 0, tensor n (stream
+  s) also draws, from ``default_rng([seed, 8 + s])``, a uniform mask and
+  N(0, 1) values, and adds ``outlier_sd`` x value where mask < rate (before
+  the dtype rounding): x = z + outlier_sd * o * Bernoulli(rate).  The pages
+  give no input distribution for the FP8 comparison; this one puts rare
+  coordinates an order of magnitude above the rest, the situation the
+  pages say the rotation is for;
+* the FP8 rotation's sign vector: ``rotation_signs`` draws d values of
+  +-1 from ``default_rng([seed, 16])``.
 """
 from __future__ import annotations
 
@@ -61,6 +70,8 @@ class Workload:
     block_mask: Optional[np.ndarray] = field(default=None, repr=False)
     H_kv: Optional[int] = None                # K/V heads (grouped-query); None -> H
     window: int = 0                           # causal sliding window of keys (0 = none)
+    outlier_rate: float = 0.0                 # probability of an outlier entry
+    outlier_sd: float = 0.0                   # outlier standard deviation
 
     def __post_init__(self):
         if self.seqlen_range is not None and self.seqlens is None:
@@ -83,19 +94,31 @@ class Workload:
         return replace(self, **kw)
 
 
-def _draw(shape, seed, stream, scale, dtype):
+def _draw(shape, seed, stream, scale, dtype, outlier_rate=0.0, outlier_sd=0.0):
     rng = np.random.default_rng([seed, stream])
     x = rng.standard_normal(size=shape, dtype=np.float32)
+    if outlier_rate > 0.0:
+        ro = np.random.default_rng([seed, 8 + stream])
+        hit = ro.random(size=shape) < outlier_rate
+        o = ro.standard_normal(size=shape, dtype=np.float32)
+        x = x + np.where(hit, np.float32(outlier_sd) * o, np.float32(0.0))
     if scale != 1.0:
         x = x * np.float32(scale)
     return torch.from_numpy(x).to(DTYPES[dtype])
+
+
+def rotation_signs(d: int, seed: int) -> np.ndarray:
+    """d random signs (int8, +-1) for the FP8 path's rotation."""
+    rng = np.random.default_rng([seed, 16])
+    return (rng.integers(0, 2, size=d) * 2 - 1).astype(np.int8)
 
 
 def make_inputs(wl: Workload, grads: bool = True):
     """q, do as [B,H,N,d] and k, v as [B,H_kv,N,d] torch CPU tensors of the storage dtype."""
     shp = (wl.B, wl.H, wl.N, wl.d)
     kshp = (wl.B, wl.hkv, wl.N, wl.d)
-    out = {n: _draw(shp if n == "q" else kshp, wl.seed, s, wl.input_scale, wl.dtype)
+    out = {n: _draw(shp if n == "q" else kshp, wl.seed, s, wl.input_scale, wl.dtype,
+                    wl.outlier_rate, wl.outlier_sd)
            for s, n in enumerate(("q", "k", "v"))}
     if grads:
         out["do"] = _draw(shp, wl.seed, 3, wl.input_scale, wl.dtype)
@@ -129,4 +152,12 @@ CONFIGS = {
     # "Lo que Flash forward no hace"); same FLOPs as the d = 64 workload
     "gpt2_medium_d128_causal": Workload("gpt2_medium_d128_causal", B=64, H=8, N=1024, d=128,
                                         dtype="bf16", causal=True, seed=20268),
+    # FP8 forward (living-dl-book, section 10; marketmaker.cc, "FA3"): the
+    # GPT-2-medium shape, bf16 inputs quantised to E4M3 per 128-row block
+    # after the random rotation
+    "gpt2_medium_causal_fp8": Workload("gpt2_medium_causal_fp8", B=64, H=16, N=1024, dtype="bf16",
+                                       causal=True, seed=20269),
+    # FP8 error study: N(0, 1) plus 0.1 % outliers of standard deviation 10
+    "outliers_fp8": Workload("outliers_fp8", B=1, H=4, N=2048, dtype="bf16", seed=20270,
+                             outlier_rate=1e-3, outlier_sd=10.0),
 }

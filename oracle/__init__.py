@@ -19,7 +19,10 @@ pages by eye rather than to be fast:
                      algorithms, for the pages' byte-accounting worked numbers.
 * ``masks``       -- the causal / sliding-window / key-padding / block-sparse
                      mask definitions.
+* ``fp8``         -- the FP8 forward: E4M3 rounding, the random Hadamard
+                     rotation, block (or per-tensor) quantisation and the
+                     online-softmax forward on the quantised inputs.
 
 Parity status of each function is stated in its own docstring ("pinned by ...").
 """
-from . import philox, masks, attention, tiled, traffic  # noqa: F401
+from . import philox, masks, attention, tiled, traffic, fp8  # noqa: F401
