@@ -30,6 +30,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fwd+bwd attention TFLOP/s & % of BF16 tensor peak, GPT-2-medium shape"
+METRIC_FP8 = "FP8 (E4M3) attention forward TFLOP/s, quantiser included"
 
 
 def visible_pairs(wl) -> int:
@@ -148,9 +149,17 @@ def replica_value(ws, step_flops, ms_max):
     return ws * step_flops / (ms_max * 1e-3) / 1e12
 
 
+def is_fp8(wl) -> bool:
+    return wl.name.endswith("_fp8")
+
+
 def oracle_sample(wl, budget_s, inputs=None):
-    """Time the float64 oracle (as it stands) on whole heads of `wl` for ~budget_s."""
+    """Time the float64 oracle (as it stands) on whole heads of `wl` for ~budget_s.
+
+    FP8 workloads time the oracle's FP8 forward (quantise one head, then the
+    forward on its codes); the others time the exact forward + backward."""
     from oracle import attention as A
+    from oracle import fp8 as F
     from exact_io_aware_tiled_gb300 import workloads as W
     spec = A.Spec(B=wl.B, H=wl.H, N=wl.N, d=wl.d, causal=wl.causal,
                   seqlens_k=None if wl.seqlens is None else np.asarray(wl.seqlens),
@@ -160,12 +169,19 @@ def oracle_sample(wl, budget_s, inputs=None):
     one = wl.with_(B=1, H=1, H_kv=None, seqlens=None if wl.seqlens is None else wl.seqlens[:1])
     inp = W.make_inputs(one) if inputs is None else inputs
     q, k, v, do = (inp[n][0, 0].float().numpy().astype(np.float64) for n in ("q", "k", "v", "do"))
-    head_flops = 2.5 * 4 * wl.d * visible_pairs(one)
+    fp8 = is_fp8(wl)
+    head_flops = (1.0 if fp8 else 2.5) * 4 * wl.d * visible_pairs(one)
+    signs = W.rotation_signs(wl.d, wl.seed)
     t0 = time.perf_counter()
     heads = 0
     while True:
-        A.head_forward(spec, 0, 0, q, k, v)
-        A.head_backward(spec, 0, 0, q, k, v, do)
+        if fp8:
+            qz = [F.quantize(x[None, None], signs) for x in (q, k, v)]
+            F.head_forward(spec, 0, 0, qz[0][0][0, 0], qz[0][1][0, 0], qz[1][0][0, 0], qz[1][1][0, 0],
+                           qz[2][0][0, 0], qz[2][1][0, 0], signs)
+        else:
+            A.head_forward(spec, 0, 0, q, k, v)
+            A.head_backward(spec, 0, 0, q, k, v, do)
         heads += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -202,7 +218,8 @@ def run_reference(args, wl):
         "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "causal": wl.causal,
                    "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
-                         "sample": "one (b=0,h=0) head fwd+bwd per step, float64 numpy, %d heads total" % heads_total},
+                         "sample": "one (b=0,h=0) head %s per step, float64 numpy, %d heads total"
+                                   % ("FP8 quantise + forward" if is_fp8(wl) else "fwd+bwd", heads_total)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -248,22 +265,33 @@ def main():
               seqlens_k=None if wl.seqlens is None else torch.from_numpy(np.asarray(wl.seqlens, np.int32)).to(dev),
               block_mask=None if wl.block_mask is None else torch.from_numpy(wl.block_mask.astype(np.uint8)).to(dev))
     pairs = visible_pairs(wl)
+    fp8 = is_fp8(wl)
     fwd_flops = 4.0 * wl.d * pairs
-    bwd_flops = 10.0 * wl.d * pairs
-    step_flops_headline = 2.5 * fwd_flops
+    bwd_flops = 0.0 if fp8 else 10.0 * wl.d * pairs
+    # FP8 workloads are forward only (quantise + forward): their step counts the forward FLOPs
+    step_flops_headline = fwd_flops if fp8 else 2.5 * fwd_flops
     step_flops_exec = fwd_flops + bwd_flops
     stream = torch.cuda.current_stream(dev)
+    if fp8:
+        kw8 = {k_: v_ for k_, v_ in kw.items() if k_ not in ("dropout_p", "seed", "offset")}
+        signs = torch.from_numpy(W.rotation_signs(wl.d, wl.seed)).to(dev)
+        fp8_buf = torch.empty(fa.fp8_layout(fa.make_params(t["q"], k=t["k"]))["total"], device=dev,
+                              dtype=torch.uint8)
 
-    def step(prof_f=None, prof_b=None):
-        o, lse = fa.fwd(t["q"], t["k"], t["v"], prof=prof_f, **kw)
-        dq, dk, dv = fa.bwd(t["q"], t["k"], t["v"], o, t["do"], lse, prof=prof_b, **kw)
+    def step(prof_f=None, prof_b=None, src=None):
+        src = t if src is None else src
+        if fp8:
+            o, lse = fa.fwd_fp8(src["q"], src["k"], src["v"], signs=signs, prof=prof_f, buf=fp8_buf, **kw8)
+            return o, lse, None
+        o, lse = fa.fwd(src["q"], src["k"], src["v"], prof=prof_f, **kw)
+        dq, dk, dv = fa.bwd(src["q"], src["k"], src["v"], o, src["do"], lse, prof=prof_b, **kw)
         return o, lse, dq
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    st_f = fa.check_status(fa.fwd.last_workspace)
-    st_b = fa.check_status(fa.bwd.last_workspace)
+    st_f = fa.check_status(fa.fwd_fp8.last_workspace if fp8 else fa.fwd.last_workspace)
+    st_b = 0 if fp8 else fa.check_status(fa.bwd.last_workspace)
     if st_f or st_b:
         raise SystemExit("device status after warm-up: fwd %d bwd %d" % (st_f, st_b))
 
@@ -289,7 +317,7 @@ def main():
     clocks = clk.stop()
     ms = e0.elapsed_time(e1) / K
     fwd_ms = sum(a.elapsed_time(b) for a, b in evf) / K
-    bwd_ms = sum(a.elapsed_time(b) for a, b in evb) / K
+    bwd_ms = 0.0 if fp8 else sum(a.elapsed_time(b) for a, b in evb) / K
     ms_max = _max_over_ranks(ms, ws, dev)
 
     # end to end: pinned host inputs -> device, fwd + bwd, O, LSE and the
@@ -300,13 +328,15 @@ def main():
     # sets, two host output sets).
     e2e = None
     if not args.no_e2e:
-        hp = {k: v.pin_memory() for k, v in host.items()}
+        ins = ("q", "k", "v") if fp8 else ("q", "k", "v", "do")
+        outs = ("o",) if fp8 else ("o", "dq", "dk", "dv")
+        hp = {k: host[k].pin_memory() for k in ins}
         kv_like = lambda n: "k" if n in ("dk", "dv") else "q"
-        hout = [{n: torch.empty_like(hp[kv_like(n)]).pin_memory() for n in ("o", "dq", "dk", "dv")}
+        hout = [{n: torch.empty_like(hp[kv_like(n)]).pin_memory() for n in outs}
                 for _ in range(2)]
         for ho in hout:
             ho["lse"] = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32).pin_memory()
-        dsets = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
+        dsets = [{k: torch.empty_like(hp[k], device=dev) for k in ins} for _ in range(2)]
         h2d = sum(v.numel() * v.element_size() for v in hp.values())
         d2h = sum(v.numel() * v.element_size() for v in hout[0].values())
         s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
@@ -323,12 +353,17 @@ def main():
                 ev_in[x].record(s_in)
             s_cmp.wait_event(ev_in[x])
             with torch.cuda.stream(s_cmp):
-                o, lse = fa.fwd(d["q"], d["k"], d["v"], **kw)
-                dq, dk, dv = fa.bwd(d["q"], d["k"], d["v"], o, d["do"], lse, **kw)
+                if fp8:
+                    o, lse = fa.fwd_fp8(d["q"], d["k"], d["v"], signs=signs, **kw8)
+                    res = (("o", o), ("lse", lse))
+                else:
+                    o, lse = fa.fwd(d["q"], d["k"], d["v"], **kw)
+                    dq, dk, dv = fa.bwd(d["q"], d["k"], d["v"], o, d["do"], lse, **kw)
+                    res = (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))
                 ev_cmp[x].record(s_cmp)
             s_out.wait_event(ev_cmp[x])
             with torch.cuda.stream(s_out):
-                for n, t_ in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+                for n, t_ in res:
                     hout[x][n].copy_(t_, non_blocking=True)
                     t_.record_stream(s_out)
 
@@ -356,7 +391,12 @@ def main():
     kern_flops = bwd_flops if dominant == "bwd" else fwd_flops
     achieved = kern_flops / (kern_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops_sustained"])
-    traffic = _recorded_traffic(wl.name, dominant)
+    peak_src = "%s bf16_tflops_sustained" % peak_kind
+    if fp8:     # E4M3 products: the bf16 peak x the nominal dense FP8 / BF16 ratio (4.5 / 2.25)
+        peak *= 2.0
+        peak_src = "%s bf16_tflops_sustained x 2 (nominal fp8 / bf16 dense ratio)" % peak_kind
+    kern_name = ("attn_%s_tc" % dominant) if not fp8 else "attn_fwd_fp8"
+    traffic = _recorded_traffic(wl.name, "fwd_fp8" if fp8 else dominant)
 
     if rank != 0:
         return
@@ -364,12 +404,13 @@ def main():
     if ws == 1 and args.cpu_budget > 0:
         v, heads, dt = oracle_sample(wl, args.cpu_budget)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
-               "sample": "%d whole (b=0,h=0) heads fwd+bwd in %.1f s, float64 numpy" % (heads, dt)}
+               "sample": "%d whole (b=0,h=0) heads %s in %.1f s, float64 numpy"
+                         % (heads, "FP8 quantise + forward" if fp8 else "fwd+bwd", dt)}
     value = replica_value(ws, step_flops_headline, ms_max)
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "metric": METRIC_FP8 if fp8 else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": wl.dtype, "data": "synthetic",
+        "dtype": "e4m3 (from %s inputs)" % wl.dtype if fp8 else wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "H_kv": wl.hkv, "N": wl.N, "d": wl.d,
                    "causal": wl.causal, "window": wl.window,
                    "dropout_p": wl.dropout_p, "parallelism": "replicas" if ws > 1 else "single",
@@ -378,9 +419,9 @@ def main():
         "pct_of_bf16_peak": 100.0 * value / float(peaks["bf16_tflops_sustained"]) / ws,
         "value_executed_flops": replica_value(ws, step_flops_exec, ms_max),
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-        "roofline": {"kernel": "attn_%s_tc" % dominant, "bound": "tensor", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": kern_name, "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": "%s bf16_tflops_sustained" % peak_kind},
+                     "peak_source": peak_src},
         "roofline_fwd": {"achieved": fwd_flops / (fwd_ms * 1e-3) / 1e12, "peak": peak,
                          "frac": fwd_flops / (fwd_ms * 1e-3) / 1e12 / peak},
         "clocks": clocks,
@@ -393,7 +434,10 @@ def main():
 
 def _launches_per_step(wl):
     # fwd: [block lists] + attention; bwd: [block lists] + prep + attention + dq convert (16-bit)
+    # FP8: quantiser (one pass with block scales) + [block lists] + attention
     sparse = 1 if wl.block_mask is not None else 0
+    if is_fp8(wl):
+        return 1 + sparse + 1
     fwd = sparse + 1
     bwd = sparse + 2 + (0 if wl.dtype == "f32" else 1)
     return fwd + bwd
@@ -403,7 +447,10 @@ def _source_hash(which):
     import hashlib
     m = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_io_aware_tiled_gb300", "csrc")
-    files = ["%s_tc.cu" % which, "common.cuh"] + (["bwd_items.cuh"] if which == "bwd" else [])
+    if which == "fwd_fp8":
+        files = ["fwd_fp8.cu", "fp8.cuh", "fwd_plan.cuh", "common.cuh"]
+    else:
+        files = ["%s_tc.cu" % which, "common.cuh"] + (["bwd_items.cuh"] if which == "bwd" else [])
     for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             m.update(fh.read())

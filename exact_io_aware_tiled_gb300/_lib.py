@@ -21,7 +21,8 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_WORKSPA
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 EXPORTED = ["fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd", "fa_bwd_noalloc",
-            "fa_check_status", "fa_dropout_mask", "fa_selftest_wait_timeout", "fa_status_string", "fa_version"]
+            "fa_check_status", "fa_dropout_mask", "fa_selftest_wait_timeout", "fa_status_string", "fa_version",
+            "fa_fp8_buffer_layout", "fa_fp8_quantize", "fa_fwd_fp8"]
 
 
 class fa_params(ctypes.Structure):
@@ -42,6 +43,14 @@ class fa_params(ctypes.Structure):
         ("kv_stride_b", ctypes.c_int64), ("kv_stride_h", ctypes.c_int64), ("kv_stride_n", ctypes.c_int64),
         ("window", ctypes.c_int32),
     ]
+
+
+class fa_fp8_params(ctypes.Structure):
+    _fields_ = [("per_tensor", ctypes.c_int32), ("signs", ctypes.c_void_p)]
+
+
+class fa_fp8_layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("q8", "k8", "v8t", "sq", "sk", "sv", "amax", "total")]
 
 
 class FAError(RuntimeError):
@@ -80,6 +89,13 @@ def load():
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_version.argtypes = []
     lib.fa_version.restype = ctypes.c_int32
+    F = ctypes.POINTER(fa_fp8_params)
+    lib.fa_fp8_buffer_layout.argtypes = [P, ctypes.POINTER(fa_fp8_layout)]
+    lib.fa_fp8_buffer_layout.restype = ctypes.c_int
+    lib.fa_fp8_quantize.argtypes = [P, F, vp, vp, vp, vp, sz, vp]
+    lib.fa_fp8_quantize.restype = ctypes.c_int
+    lib.fa_fwd_fp8.argtypes = [P, F, vp, sz, vp, vp, vp, sz, vp]
+    lib.fa_fwd_fp8.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -278,3 +294,92 @@ def bwd_noalloc(q, k, v, o, do, lse, *, causal=False, seqlens_k=None, dropout_p=
     if st != FA_OK:
         raise FAError(st, "fa_bwd_noalloc")
     return dq, dk, dv
+
+
+def _fp8_args(q, signs, per_tensor):
+    f = fa_fp8_params()
+    f.per_tensor = 1 if per_tensor else 0
+    sg = None
+    if signs is not None:
+        sg = torch.as_tensor(signs).to(device=q.device, dtype=torch.int8).contiguous()
+        if sg.numel() != q.shape[3]:
+            raise ValueError("signs must have d entries")
+        f.signs = sg.data_ptr()
+    return f, sg
+
+
+def fp8_layout(p: fa_params) -> dict:
+    """Byte offsets of the quantised buffer's parts (fa_fp8_buffer_layout)."""
+    lay = fa_fp8_layout()
+    st = load().fa_fp8_buffer_layout(ctypes.byref(p), ctypes.byref(lay))
+    if st != FA_OK:
+        raise FAError(st, "fa_fp8_buffer_layout")
+    return {n: int(getattr(lay, n)) for n, _ in fa_fp8_layout._fields_}
+
+
+def fp8_views(buf: torch.Tensor, lay: dict, B, H, H_kv, N, d=64) -> dict:
+    """The quantised buffer's parts as tensors (views, no copies)."""
+    nt = -(-N // 128)
+    npad = nt * 128
+
+    def u8(off, shape):
+        n = math.prod(shape)
+        return buf[off:off + n].view(shape)
+
+    def f32(off, shape):
+        n = math.prod(shape)
+        return buf[off:off + 4 * n].view(torch.float32).view(shape)
+
+    return dict(q8=u8(lay["q8"], (B, H, N, d)), k8=u8(lay["k8"], (B, H_kv, N, d)),
+                v8t=u8(lay["v8t"], (B, H_kv, d, npad)), sq=f32(lay["sq"], (B, H, nt)),
+                sk=f32(lay["sk"], (B, H_kv, nt)), sv=f32(lay["sv"], (B, H_kv, nt)))
+
+
+def fp8_quantize(q, k, v, *, signs=None, per_tensor=False, stream=None, buf=None):
+    """Quantise q, k, v to E4M3 (fa_fp8_quantize): returns (buffer, views)."""
+    _check(q)
+    (q,), (k, v) = _layouts([q], [k, v])
+    lib = load()
+    p = make_params(q, k=k)
+    f, sg = _fp8_args(q, signs, per_tensor)
+    lay = fp8_layout(p)
+    if buf is None:
+        buf = torch.empty(lay["total"], device=q.device, dtype=torch.uint8)
+    st = lib.fa_fp8_quantize(ctypes.byref(p), ctypes.byref(f), _ptr(q), _ptr(k), _ptr(v), _ptr(buf), buf.numel(),
+                             _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fp8_quantize")
+    fp8_quantize.last_signs = sg       # keep the device copy alive until the stream has used it
+    return buf, fp8_views(buf, lay, q.shape[0], q.shape[1], k.shape[1], q.shape[2], q.shape[3])
+
+
+def fwd_fp8(q, k, v, *, signs=None, per_tensor=False, causal=False, seqlens_k=None, block_mask=None, scale=None,
+            window=0, return_o_f32=False, return_quantized=False, stream=None, prof=None, buf=None):
+    """FP8 forward (fa_fp8_quantize + fa_fwd_fp8): O (dtype of q), LSE, and
+    optionally the float32 O before rounding and the quantised operands."""
+    _check(q)
+    (q,), (k, v) = _layouts([q], [k, v])
+    lib = load()
+    seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
+    B, H, N, d = q.shape
+    f, sg = _fp8_args(q, signs, per_tensor)
+    buf, views = fp8_quantize(q, k, v, signs=sg, per_tensor=per_tensor, stream=stream, buf=buf)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    o32 = torch.empty((B, H, N, d), device=q.device, dtype=torch.float32) if return_o_f32 else None
+    p = make_params(q, k=k, causal=causal, seqlens_k=seqlens_k, block_mask=block_mask, scale=scale, o_f32=o32,
+                    prof=prof, window=window)
+    wsz = lib.fa_fwd_workspace_size(ctypes.byref(p))
+    ws = torch.empty(wsz, device=q.device, dtype=torch.uint8)
+    st = lib.fa_fwd_fp8(ctypes.byref(p), ctypes.byref(f), _ptr(buf), buf.numel(), _ptr(o), _ptr(lse), _ptr(ws), wsz,
+                        _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_fp8")
+    fwd_fp8.last_workspace = ws
+    fwd_fp8.last_signs = sg
+    out = (o, lse)
+    if return_o_f32:
+        out = out + (o32,)
+    if return_quantized:
+        out = out + (views,)
+    return out

@@ -199,6 +199,59 @@ struct ProfScope {
   }
 };
 
+// ---- FP8 forward -------------------------------------------------------------
+struct Fp8Layout {
+  size_t q8 = 0, k8 = 0, v8t = 0, sq = 0, sk = 0, sv = 0, amax = 0, total = 0;
+  int nt = 0, npad = 0;
+};
+
+Fp8Layout fp8_layout(const fa_params* p) {
+  Fp8Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  const int hkv = hkv_of(p);
+  L.nt = (p->N + kTile - 1) / kTile;
+  L.npad = L.nt * kTile;
+  const size_t rq = (size_t)p->B * p->H, rk = (size_t)p->B * hkv;
+  L.q8 = take(rq * p->N * p->d);
+  L.k8 = take(rk * p->N * p->d);
+  L.v8t = take(rk * p->d * L.npad);
+  L.sq = take(rq * L.nt * sizeof(float));
+  L.sk = take(rk * L.nt * sizeof(float));
+  L.sv = take(rk * L.nt * sizeof(float));
+  L.amax = take(4 * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+// What the FP8 path supports on top of check_params.
+fa_status check_fp8(const fa_params* p, const fa_fp8_params* f) {
+  fa_status s = check_params(p);
+  if (s != FA_OK) return s;
+  if (f == nullptr) return FA_ERR_INVALID_ARG;
+  if (p->dtype == FA_DT_F32 || p->d != 64 || p->dropout_p > 0.f) return FA_ERR_UNSUPPORTED;
+  if (f->per_tensor != 0 && f->per_tensor != 1) return FA_ERR_INVALID_ARG;
+  if (f->signs != nullptr && !aligned16(f->signs)) return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
+// 4-D byte map: dims (d0, d1, d2, d3), byte strides of dims 1-3, box (b0, b1, 1, 1).
+fa_status map_u8(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[4], const cuuint64_t (&strides)[3],
+                 cuuint32_t b0, cuuint32_t b1, CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return FA_ERR_CUDA;
+  cuuint32_t box[4] = {b0, b1, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -350,6 +403,89 @@ fa_status fa_selftest_wait_timeout(void* ws, int32_t* out, uint64_t* out_ns, voi
   return cuda_status(e);
 }
 
+fa_status fa_fp8_buffer_layout(const fa_params* p, fa_fp8_layout* out) {
+  if (p == nullptr || out == nullptr || p->B < 1 || p->H < 1 || p->N < 1 || p->d < 1) return FA_ERR_INVALID_ARG;
+  const int hkv = hkv_of(p);
+  if (hkv < 1 || p->H % hkv != 0) return FA_ERR_INVALID_ARG;
+  const Fp8Layout L = fp8_layout(p);
+  out->q8 = L.q8; out->k8 = L.k8; out->v8t = L.v8t;
+  out->sq = L.sq; out->sk = L.sk; out->sv = L.sv; out->amax = L.amax;
+  out->total = L.total;
+  return FA_OK;
+}
+
+fa_status fa_fp8_quantize(const fa_params* p, const fa_fp8_params* f, const void* q, const void* k, const void* v,
+                          void* buf, size_t buf_bytes, void* stream) {
+  fa_status s = check_fp8(p, f);
+  if (s != FA_OK) return s;
+  if (!q || !k || !v) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FA_ERR_MISALIGNED;
+  const Fp8Layout L = fp8_layout(p);
+  if (buf == nullptr || buf_bytes < L.total || !aligned16(buf)) return FA_ERR_WORKSPACE;
+  uint8_t* w = static_cast<uint8_t*>(buf);
+  const int hkv = hkv_of(p);
+  Fp8QuantArgs a{};
+  a.src[0] = q; a.src[1] = k; a.src[2] = v;
+  a.st[0] = strides_of(p); a.st[1] = a.st[2] = kv_strides_of(p);
+  a.heads[0] = p->H; a.heads[1] = a.heads[2] = hkv;
+  a.dst[0] = w + L.q8; a.dst[1] = w + L.k8; a.dst[2] = w + L.v8t;
+  a.scale[0] = reinterpret_cast<float*>(w + L.sq);
+  a.scale[1] = reinterpret_cast<float*>(w + L.sk);
+  a.scale[2] = reinterpret_cast<float*>(w + L.sv);
+  a.amax = reinterpret_cast<float*>(w + L.amax);
+  a.signs = f->signs;
+  a.B = p->B; a.N = p->N; a.nt = L.nt; a.npad = L.npad;
+  return cuda_status(launch_fp8_quantize(p->dtype, a, f->per_tensor, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_fwd_fp8(const fa_params* p, const fa_fp8_params* f, const void* buf, size_t buf_bytes, void* o,
+                     float* lse, void* ws, size_t ws_bytes, void* stream) {
+  fa_status s = check_fp8(p, f);
+  if (s != FA_OK) return s;
+  if (!o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
+  const Fp8Layout Q = fp8_layout(p);
+  if (buf == nullptr || buf_bytes < Q.total || !aligned16(buf)) return FA_ERR_WORKSPACE;
+  const Layout L = layout(p, false);
+  if (ws == nullptr || ws_bytes < L.total || !aligned16(ws)) return FA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const uint8_t* qb = static_cast<const uint8_t*>(buf);
+  const int hkv = hkv_of(p);
+
+  FwdArgs a{};
+  a.B = p->B; a.H = p->H; a.N = p->N;
+  a.group = p->H / hkv;
+  a.nq = L.nq;
+  a.npairs = (L.nq + 1) / 2;
+  a.scale_log2 = scale_of(p) * 1.4426950408889634f;
+  a.mask = mask_of(p, L, w);
+  a.drop = dropout_of(p);
+  a.lse = lse;
+  a.o_f32 = p->o_f32;
+  a.status = reinterpret_cast<int*>(w + L.status);
+  a.f8.sq = reinterpret_cast<const float*>(qb + Q.sq);
+  a.f8.sk = reinterpret_cast<const float*>(qb + Q.sk);
+  a.f8.sv = reinterpret_cast<const float*>(qb + Q.sv);
+  a.f8.signs = f->signs;
+  a.f8.nt = Q.nt;
+  a.f8.o_bf16 = p->dtype == FA_DT_BF16 ? 1 : 0;
+
+  const cuuint64_t N = (cuuint64_t)p->N, npad = (cuuint64_t)Q.npad, H = (cuuint64_t)p->H, Hk = (cuuint64_t)hkv;
+  CUtensorMap mq, mk, mv, mo;
+  if ((s = map_u8(&mq, qb + Q.q8, {64, N, H, (cuuint64_t)p->B}, {64, 64 * N, 64 * N * H}, 64, kTile,
+                  CU_TENSOR_MAP_SWIZZLE_64B)) != FA_OK ||
+      (s = map_u8(&mk, qb + Q.k8, {64, N, Hk, (cuuint64_t)p->B}, {64, 64 * N, 64 * N * Hk}, 64, kTile,
+                  CU_TENSOR_MAP_SWIZZLE_64B)) != FA_OK ||
+      (s = map_u8(&mv, qb + Q.v8t, {npad, 64, Hk, (cuuint64_t)p->B}, {npad, 64 * npad, 64 * npad * Hk}, kTile, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B)) != FA_OK ||
+      (s = map16(&mo, o, p, p->H, strides_of(p))) != FA_OK)
+    return s;
+  if ((s = prepare_common(p, L, w, st)) != FA_OK) return s;
+  ProfScope prof(p, st);
+  return cuda_status(launch_fwd_fp8(mq, mk, mv, mo, a, st));
+}
+
 const char* fa_status_string(fa_status s) {
   switch (s) {
     case FA_OK: return "FA_OK";
@@ -363,6 +499,6 @@ const char* fa_status_string(fa_status s) {
   return "FA_ERR_UNKNOWN";
 }
 
-int32_t fa_version(void) { return 101; }
+int32_t fa_version(void) { return 102; }
 
 }  // extern "C"

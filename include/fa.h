@@ -222,11 +222,74 @@ fa_status fa_dropout_mask(const fa_params *p, int32_t b, int32_t h, int32_t row0
  * ------------------------------------------------------------------------- */
 fa_status fa_selftest_wait_timeout(void *ws, int32_t *out, uint64_t *out_ns, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * FP8 forward (ABI 1.2).
+ * FlashAttention-3's low-precision path (living-dl-book, "Atencao Eficiente
+ * em Escala", section 10; marketmaker.cc, "FA3: Mecanica da tremonha", item
+ * 3): Q, K and V are quantised to FP8 one tile at a time, with one scale per
+ * tile, after a random Hadamard-style rotation of every row that spreads
+ * outlying coordinates; the rotation is undone after the products.  Here:
+ *   - FP8 is E4M3 (largest finite 448), round to nearest even, saturating;
+ *   - the rotation is M = diag(signs) H_d / sqrt(d) (H_d the Sylvester
+ *     Hadamard matrix); Q, K and V rows are all rotated; the scores are
+ *     unchanged (M M^T = I) and O is rotated back, O = O' M^T;
+ *   - a block is 128 rows x d of one head, scale = amax / 448, codes =
+ *     E4M3(x * (448 / amax)); per_tensor = 1 uses the whole tensor's amax
+ *     for every block and is the pages' baseline;
+ *   - both products run in E4M3 on the tensor cores; the probabilities of
+ *     key tile t are rounded to E4M3 as E4M3(exp(S - m) * 256 * sv_t / SV)
+ *     with m the running row max (the accumulator is rescaled whenever m
+ *     grows), sv_t the V scale of tile t and SV the largest V scale of the
+ *     head; the row sum uses the unrounded probabilities;
+ *   - head dimension 64, float16 or bfloat16 inputs and output; causal,
+ *     key padding, block-sparse masks, the sliding window and grouped K/V
+ *     heads as in fa_fwd; dropout returns FA_ERR_UNSUPPORTED.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int32_t per_tensor;        /* 0: one scale per 128-row block; 1: per tensor   */
+  const int8_t *signs;       /* device int8 [d] of +1 / -1, 16-byte aligned:
+                                rotate rows by diag(signs) H_d / sqrt(d);
+                                NULL: no rotation                              */
+} fa_fp8_params;
+
+/* Byte offsets (multiples of 256) of the parts of the quantised buffer:
+ *   q8  : uint8 [B,H,N,d]      E4M3 codes of the (rotated) Q rows
+ *   k8  : uint8 [B,H_kv,N,d]   of K
+ *   v8t : uint8 [B,H_kv,d,Np]  of V, transposed (keys contiguous), Np = N
+ *                              rounded up to 128, zero on keys >= N
+ *   sq  : float [B,H,nt]       dequantisation scale of each 128-row tile,
+ *   sk, sv : float [B,H_kv,nt] nt = ceil(N / 128)
+ *   amax: float [4]            scratch of the per-tensor mode
+ * total is the buffer size. */
+typedef struct {
+  size_t q8, k8, v8t, sq, sk, sv, amax, total;
+} fa_fp8_layout;
+
+/* Fills *out for the problem p (a pure host function). */
+fa_status fa_fp8_buffer_layout(const fa_params *p, fa_fp8_layout *out);
+
+/* fa_fp8_quantize -- quantises q, k, v ([B,H,N,d] / [B,H_kv,N,d] 16-bit
+ * tensors with the strides of p) into buf (device, 16-byte aligned,
+ * buf_bytes >= layout.total).  The float32 order of operations is fixed:
+ * sign flip, butterfly stages h = 1, 2, ..., d/2, multiply by 1/sqrt(d),
+ * block amax, inv = 448 / amax, x * inv, E4M3 rounding. */
+fa_status fa_fp8_quantize(const fa_params *p, const fa_fp8_params *f, const void *q, const void *k,
+                          const void *v, void *buf, size_t buf_bytes, void *stream);
+
+/* fa_fwd_fp8 -- the forward pass on a buffer fa_fp8_quantize filled with
+ * the same p and f (f->signs rotates O back).  o: device [B,H,N,d] output in
+ * p->dtype with p's strides; lse: device float32 [B,H,N] (natural log of
+ * the scores of the dequantised operands); ws: ws_bytes >=
+ * fa_fwd_workspace_size(p).  p->o_f32, if set, receives O before its final
+ * rounding. */
+fa_status fa_fwd_fp8(const fa_params *p, const fa_fp8_params *f, const void *buf, size_t buf_bytes,
+                     void *o, float *lse, void *ws, size_t ws_bytes, void *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *fa_status_string(fa_status s);
 
 /* Library ABI version (major * 100 + minor): 101 adds H_kv, kv_stride_*
- * and window to fa_params. */
+ * and window to fa_params; 102 adds the FP8 forward. */
 int32_t fa_version(void);
 
 #ifdef __cplusplus

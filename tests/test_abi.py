@@ -78,7 +78,7 @@ def _params(**kw):
 def test_status_strings(lib):
     assert lib.fa_status_string(0) == b"FA_OK"
     assert lib.fa_status_string(6) == b"FA_ERR_TIMEOUT"
-    assert lib.fa_version() >= 101
+    assert lib.fa_version() >= 102
 
 
 def test_workspace_sizes(lib):
@@ -150,3 +150,68 @@ def test_binding_never_imports_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), f
                 assert "oracle." not in src or f.endswith((".cu", ".cuh", ".h")), f
+
+
+# ---- FP8 forward (ABI 1.2) ---------------------------------------------------
+def test_fp8_structs_match_c(tmp_path):
+    from exact_io_aware_tiled_gb300._lib import fa_fp8_layout, fa_fp8_params
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    prog = ['#include <stdio.h>', '#include <stddef.h>', '#include "fa.h"', 'int main(void){']
+    for st in (fa_fp8_params, fa_fp8_layout):
+        prog.append('printf("%%zu\\n", sizeof(%s));' % st.__name__)
+        prog += ['printf("%%zu\\n", offsetof(%s, %s));' % (st.__name__, f) for f, _ in st._fields_]
+    prog += ['return 0;}']
+    c = tmp_path / "fp8layout.c"
+    c.write_text("\n".join(prog))
+    exe = tmp_path / "fp8layout"
+    subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), str(c), "-o", str(exe)], check=True)
+    vals = iter(int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split())
+    for st in (fa_fp8_params, fa_fp8_layout):
+        assert next(vals) == ctypes.sizeof(st)
+        for f, _ in st._fields_:
+            assert getattr(st, f).offset == next(vals), f
+
+
+def test_fp8_buffer_layout(lib):
+    from exact_io_aware_tiled_gb300._lib import fa_fp8_layout
+    p = _params(H=4, H_kv=2, kv_stride_b=2 * 200 * 64, kv_stride_h=200 * 64, kv_stride_n=64)
+    lay = fa_fp8_layout()
+    assert lib.fa_fp8_buffer_layout(ctypes.byref(p), ctypes.byref(lay)) == 0
+    parts = [lay.q8, lay.k8, lay.v8t, lay.sq, lay.sk, lay.sv, lay.amax, lay.total]
+    assert parts == sorted(parts) and all(x % 256 == 0 for x in parts)
+    assert lay.k8 - lay.q8 >= 2 * 4 * 200 * 64            # Q codes: one byte per element
+    assert lay.sq - lay.v8t >= 2 * 2 * 64 * 256           # V^T codes: keys padded to 256
+    assert lay.sk - lay.sq >= 2 * 4 * 2 * 4               # two 128-row tiles per head
+    assert lib.fa_fp8_buffer_layout(None, ctypes.byref(lay)) == 1
+
+
+@pytest.mark.parametrize("mut,fmut,code", [
+    (dict(dtype=0), {}, 2),           # no float32 FP8 path
+    (dict(d=128, stride_n=128, stride_h=200 * 128, stride_b=600 * 128), {}, 2),   # head dimension 64 only
+    (dict(dropout_p=0.1), {}, 2),     # no dropout in the FP8 forward
+    ({}, dict(per_tensor=2), 1),
+    ({}, dict(signs=(1 << 20) + 4), 3),
+    (dict(window=5), {}, 2),
+])
+def test_fp8_host_validation(lib, mut, fmut, code):
+    from exact_io_aware_tiled_gb300._lib import fa_fp8_params
+    p = _params(**mut)
+    f = fa_fp8_params()
+    for k, v in fmut.items():
+        setattr(f, k, v)
+    ws = ctypes.c_void_p(1 << 21)
+    assert lib.fa_fp8_quantize(ctypes.byref(p), ctypes.byref(f), FAKE, FAKE, FAKE, ws, 1 << 30, None) == code
+    assert lib.fa_fwd_fp8(ctypes.byref(p), ctypes.byref(f), ws, 1 << 30, FAKE, FAKE, ws, 1 << 30, None) == code
+
+
+def test_fp8_small_buffers_are_refused(lib):
+    from exact_io_aware_tiled_gb300._lib import fa_fp8_params
+    p = _params()
+    f = fa_fp8_params()
+    ws = ctypes.c_void_p(1 << 21)
+    assert lib.fa_fp8_quantize(ctypes.byref(p), ctypes.byref(f), FAKE, FAKE, FAKE, ws, 256, None) == 4
+    assert lib.fa_fwd_fp8(ctypes.byref(p), ctypes.byref(f), ws, 256, FAKE, FAKE, ws, 1 << 30, None) == 4
+    assert lib.fa_fwd_fp8(ctypes.byref(p), ctypes.byref(f), ws, 1 << 30, FAKE, FAKE, ws, 16, None) == 4
+    assert lib.fa_fwd_fp8(ctypes.byref(p), None, ws, 1 << 30, FAKE, FAKE, ws, 1 << 30, None) == 1
