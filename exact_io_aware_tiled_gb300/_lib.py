@@ -186,24 +186,53 @@ def _aux(seqlens_k, block_mask, q):
     return seqlens_k, block_mask
 
 
+def _outputs(out, likes):
+    """Caller-provided output tensors (checked against the shapes, dtypes and
+    devices the call would allocate), or fresh ones."""
+    if out is None:
+        return [torch.empty_like(t) if isinstance(t, torch.Tensor) else torch.empty(t[0], dtype=t[1], device=t[2])
+                for t in likes]
+    if len(out) != len(likes):
+        raise ValueError("out must hold %d tensors" % len(likes))
+    for o, t in zip(out, likes):
+        shape, dtype, device = (t.shape, t.dtype, t.device) if isinstance(t, torch.Tensor) else t
+        if tuple(o.shape) != tuple(shape) or o.dtype != dtype or o.device != torch.device(device) or \
+                not o.is_contiguous():
+            raise ValueError("out tensor %s %s does not match %s %s (contiguous)" % (tuple(o.shape), o.dtype,
+                                                                                  tuple(shape), dtype))
+    return list(out)
+
+
+def _workspace(lib_size, workspace, device):
+    """A caller-provided uint8 workspace of at least lib_size bytes, or a fresh one."""
+    if workspace is None:
+        return torch.empty(lib_size, device=device, dtype=torch.uint8)
+    if workspace.dtype != torch.uint8 or workspace.numel() < lib_size or workspace.device != device:
+        raise ValueError("workspace must be a uint8 tensor of >= %d bytes on %s" % (lib_size, device))
+    return workspace
+
+
 def fwd(q, k, v, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0, block_mask=None,
-        scale=None, return_o_f32=False, stream=None, prof=None, window=0):
+        scale=None, return_o_f32=False, stream=None, prof=None, window=0, out=None, workspace=None):
     """O, LSE (and optionally the float32 O before rounding) via fa_fwd.
 
     k, v may have fewer heads than q (grouped-query attention); ``window`` > 0
-    (with ``causal``) restricts query i to keys i - window < j <= i."""
+    (with ``causal``) restricts query i to keys i - window < j <= i.  ``out``
+    = (o, lse) and ``workspace`` (uint8, fa_fwd_workspace_size bytes) let a
+    caller reuse its own buffers instead of allocating on every call."""
     _check(q)
     (q,), (k, v) = _layouts([q], [k, v])
     lib = load()
     seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
     B, H, N, d = q.shape
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    if out is not None and not q.is_contiguous():
+        q = q.contiguous()
+    o, lse = _outputs(out, [q, ((B, H, N), torch.float32, q.device)])
     o32 = torch.empty((B, H, N, d), device=q.device, dtype=torch.float32) if return_o_f32 else None
     p = make_params(q, k=k, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
                     block_mask=block_mask, scale=scale, o_f32=o32, prof=prof, window=window)
     wsz = lib.fa_fwd_workspace_size(ctypes.byref(p))
-    ws = torch.empty(wsz, device=q.device, dtype=torch.uint8)
+    ws = _workspace(wsz, workspace, q.device)
     st = lib.fa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), wsz, _stream(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd")
@@ -212,18 +241,23 @@ def fwd(q, k, v, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=
 
 
 def bwd(q, k, v, o, do, lse, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0, block_mask=None,
-        scale=None, stream=None, prof=None, window=0):
-    """dQ, dK, dV via fa_bwd (dK, dV have the K/V heads of k, v)."""
+        scale=None, stream=None, prof=None, window=0, out=None, workspace=None):
+    """dQ, dK, dV via fa_bwd (dK, dV have the K/V heads of k, v).  ``out`` =
+    (dq, dk, dv) and ``workspace`` (uint8, fa_bwd_workspace_size bytes) let a
+    caller reuse its own buffers; the outputs must then share q's / k's
+    (contiguous) layout."""
     _check(q)
     (q, o, do), (k, v) = _layouts([q, o, do], [k, v])
+    if out is not None and (not q.is_contiguous() or not k.is_contiguous()):
+        q, o, do, k, v = (t.contiguous() for t in (q, o, do, k, v))
     lib = load()
     seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
     lse = lse.contiguous()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dq, dk, dv = _outputs(out, [q, k, v])
     p = make_params(q, k=k, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
                     block_mask=block_mask, scale=scale, prof=prof, window=window)
     wsz = lib.fa_bwd_workspace_size(ctypes.byref(p))
-    ws = torch.empty(wsz, device=q.device, dtype=torch.uint8)
+    ws = _workspace(wsz, workspace, q.device)
     st = lib.fa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
                     _ptr(dv), _ptr(ws), wsz, _stream(stream))
     if st != FA_OK:
@@ -354,23 +388,27 @@ def fp8_quantize(q, k, v, *, signs=None, per_tensor=False, stream=None, buf=None
 
 
 def fwd_fp8(q, k, v, *, signs=None, per_tensor=False, causal=False, seqlens_k=None, block_mask=None, scale=None,
-            window=0, return_o_f32=False, return_quantized=False, stream=None, prof=None, buf=None):
+            window=0, return_o_f32=False, return_quantized=False, stream=None, prof=None, buf=None, out=None,
+            workspace=None):
     """FP8 forward (fa_fp8_quantize + fa_fwd_fp8): O (dtype of q), LSE, and
-    optionally the float32 O before rounding and the quantised operands."""
+    optionally the float32 O before rounding and the quantised operands.
+    ``buf`` (the quantised buffer), ``out`` = (o, lse) and ``workspace`` let a
+    caller reuse its own buffers."""
     _check(q)
     (q,), (k, v) = _layouts([q], [k, v])
+    if out is not None and not q.is_contiguous():
+        q = q.contiguous()
     lib = load()
     seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
     B, H, N, d = q.shape
     f, sg = _fp8_args(q, signs, per_tensor)
     buf, views = fp8_quantize(q, k, v, signs=sg, per_tensor=per_tensor, stream=stream, buf=buf)
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    o, lse = _outputs(out, [q, ((B, H, N), torch.float32, q.device)])
     o32 = torch.empty((B, H, N, d), device=q.device, dtype=torch.float32) if return_o_f32 else None
     p = make_params(q, k=k, causal=causal, seqlens_k=seqlens_k, block_mask=block_mask, scale=scale, o_f32=o32,
                     prof=prof, window=window)
     wsz = lib.fa_fwd_workspace_size(ctypes.byref(p))
-    ws = torch.empty(wsz, device=q.device, dtype=torch.uint8)
+    ws = _workspace(wsz, workspace, q.device)
     st = lib.fa_fwd_fp8(ctypes.byref(p), ctypes.byref(f), _ptr(buf), buf.numel(), _ptr(o), _ptr(lse), _ptr(ws), wsz,
                         _stream(stream))
     if st != FA_OK:

@@ -20,10 +20,14 @@
 // fixed: sign flip, butterflies (stage h = 1, 2, ..., 32), multiply by 1/8,
 // amax, inv = 448 / amax (correctly rounded), x * inv, E4M3 rounding.
 //
-// One CTA of 128 threads per block; thread r owns row r.  Q and K codes are
-// written row-major ([B, heads, N, 64] bytes); V codes are written
-// transposed ([B, H_kv, 64, npad] bytes, keys contiguous, zero past N) so
-// that the P V product reads both of its operands K-major.
+// One CTA of 128 threads per block; thread r owns row r.  The block's rows
+// are loaded and stored cooperatively (consecutive threads move consecutive
+// 16-byte chunks) through shared memory, whose 16-byte chunks are XOR-
+// swizzled with the row so that the per-row accesses are free of bank
+// conflicts.  Q and K codes are written row-major ([B, heads, N, 64] bytes);
+// V codes are written transposed ([B, H_kv, 64, npad] bytes, keys
+// contiguous, zero past N) so that the P V product reads both of its
+// operands K-major.
 #include "fp8.cuh"
 
 namespace fa {
@@ -35,7 +39,9 @@ enum QuantMode { kPerBlock = 0, kAmaxOnly = 1, kPerTensor = 2 };
 template <typename T, int kMode>
 __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
   __shared__ float red[4];
-  __shared__ __align__(16) uint8_t vt[64 * kTile];   // transposed V codes of the block
+  // the block's 16-bit rows (128 x 128 bytes), later its codes: Q / K rows
+  // (128 x 64 bytes) or the transposed V codes (64 x 128 bytes)
+  __shared__ __align__(128) uint8_t tile[kTile * 128];
 
   // tensor x and block (b, head, tile) of this CTA
   int blk = (int)blockIdx.x;
@@ -57,23 +63,27 @@ __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
   const int n = t * kTile + r;
   const Strides st = a.st[x];
 
+  // cooperative load: chunk k (16 bytes) of row q goes to q * 128 + ((k ^ q) & 7) * 16
+  const T* base = static_cast<const T*>(a.src[x]) + b * st.b + h * st.h;
+  const int rows = min(kTile, a.N - t * kTile);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int idx = r + i * kTile, q = idx >> 3, k = idx & 7;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (q < rows) u = *reinterpret_cast<const uint4*>(base + (int64_t)(t * kTile + q) * st.n + k * 8);
+    *reinterpret_cast<uint4*>(tile + q * 128 + (((k ^ q) & 7) << 4)) = u;
+  }
+  __syncthreads();
   float v[64];
-  if (n < a.N) {
-    const uint4* row = reinterpret_cast<const uint4*>(static_cast<const T*>(a.src[x]) + b * st.b + h * st.h +
-                                                      (int64_t)n * st.n);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint4 u = row[j];
-      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+  for (int j = 0; j < 8; ++j) {
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + r * 128 + (((j ^ r) & 7) << 4));
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        v[8 * j + 2 * e] = Cvt<T>::lo(w4[e]);
-        v[8 * j + 2 * e + 1] = Cvt<T>::hi(w4[e]);
-      }
+    for (int e = 0; e < 4; ++e) {
+      v[8 * j + 2 * e] = Cvt<T>::lo(w4[e]);
+      v[8 * j + 2 * e + 1] = Cvt<T>::hi(w4[e]);
     }
-  } else {
-#pragma unroll
-    for (int c = 0; c < 64; ++c) v[c] = 0.f;
   }
   if (a.signs != nullptr) {
     const uint4* sp = reinterpret_cast<const uint4*>(a.signs);
@@ -101,6 +111,7 @@ __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
   if ((r & 31) == 0) red[r >> 5] = am;
   __syncthreads();
   am = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  // (the barrier above also ends every thread's reads of the 16-bit tile)
 
   float* sc = a.scale[x] + (size_t)bh * a.nt + t;
   if constexpr (kMode == kAmaxOnly) {
@@ -117,10 +128,19 @@ __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
                   __fmul_rn(v[4 * j + 3], inv));
 
   if (x < 2) {
-    if (n < a.N) {
-      uint4* dst = reinterpret_cast<uint4*>(a.dst[x] + ((size_t)bh * a.N + n) * 64);
+    // codes of row r to r * 64 + ((j ^ (r >> 1)) & 3) * 16, then cooperative stores
 #pragma unroll
-      for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4*>(tile + r * 64 + (((j ^ (r >> 1)) & 3) << 4)) =
+          make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    __syncthreads();
+    uint8_t* dst = a.dst[x] + ((size_t)bh * a.N + (size_t)t * kTile) * 64;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int idx = r + i * kTile, q = idx >> 2, k = idx & 3;
+      if (q < rows)
+        *reinterpret_cast<uint4*>(dst + q * 64 + k * 16) =
+            *reinterpret_cast<const uint4*>(tile + q * 64 + (((k ^ (q >> 1)) & 3) << 4));
     }
   } else {
     // transpose through shared memory: vt[c][r] = code c of row r.  Keys past
@@ -130,10 +150,10 @@ __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
       for (int j = 0; j < 16; ++j) w[j] = 0u;
     }
 #pragma unroll
-    for (int c = 0; c < 64; ++c) vt[c * kTile + r] = (uint8_t)((w[c >> 2] >> ((c & 3) * 8)) & 0xFFu);
+    for (int c = 0; c < 64; ++c) tile[c * kTile + r] = (uint8_t)((w[c >> 2] >> ((c & 3) * 8)) & 0xFFu);
     __syncthreads();
     const int c = r >> 1, half = r & 1;
-    const uint4* src = reinterpret_cast<const uint4*>(vt + c * kTile + half * 64);
+    const uint4* src = reinterpret_cast<const uint4*>(tile + c * kTile + half * 64);
     uint4* dst = reinterpret_cast<uint4*>(a.dst[2] + ((size_t)bh * 64 + c) * a.npad + t * kTile + half * 64);
 #pragma unroll
     for (int j = 0; j < 4; ++j) dst[j] = src[j];
