@@ -356,18 +356,26 @@ def main():
         ev_in = [torch.cuda.Event() for _ in range(2)]
         ev_cmp = [torch.cuda.Event() for _ in range(2)]
         ev_out = [torch.cuda.Event() for _ in range(2)]
+        # per-step durations of the three parts (timed loop only)
+        KE = max(6, K // 2)
+        tev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(KE)]
+        timing = [None]
 
         def e2e_step(i):
             x = i % 2
             d, do_ = dsets[x], douts[x]
+            te = timing[0][i] if timing[0] is not None else None
             s_in.wait_event(ev_cmp[x])          # step i-2 has finished reading this input set
             with torch.cuda.stream(s_in):
+                if te: te[0].record(s_in)
                 for k in d:
                     d[k].copy_(hp[k], non_blocking=True)
+                if te: te[1].record(s_in)
                 ev_in[x].record(s_in)
             s_cmp.wait_event(ev_in[x])
             s_cmp.wait_event(ev_out[x])         # step i-2's outputs have been copied out
             with torch.cuda.stream(s_cmp):
+                if te: te[2].record(s_cmp)
                 if fp8:
                     fa.fwd_fp8(d["q"], d["k"], d["v"], signs=signs, buf=buf8, out=(do_["o"], do_["lse"]),
                                workspace=ws_f, **kw8)
@@ -375,11 +383,14 @@ def main():
                     fa.fwd(d["q"], d["k"], d["v"], out=(do_["o"], do_["lse"]), workspace=ws_f, **kw)
                     fa.bwd(d["q"], d["k"], d["v"], do_["o"], d["do"], do_["lse"],
                            out=(do_["dq"], do_["dk"], do_["dv"]), workspace=ws_b, **kw)
+                if te: te[3].record(s_cmp)
                 ev_cmp[x].record(s_cmp)
             s_out.wait_event(ev_cmp[x])
             with torch.cuda.stream(s_out):
+                if te: te[4].record(s_out)
                 for n in hout[x]:
                     hout[x][n].copy_(do_[n], non_blocking=True)
+                if te: te[5].record(s_out)
                 ev_out[x].record(s_out)
 
         for i in range(4):                      # both buffer sets, twice
@@ -387,7 +398,7 @@ def main():
         torch.cuda.synchronize()
         _barrier(ws)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        KE = max(6, K // 2)
+        timing[0] = tev
         a.record(s_in)
         for i in range(KE):
             e2e_step(i)
@@ -396,8 +407,11 @@ def main():
         b.record(s_out)
         torch.cuda.synchronize()
         e2e_ms = _max_over_ranks(a.elapsed_time(b) / KE, ws, dev)
+        parts = {n: round(sum(te[j].elapsed_time(te[j + 1]) for te in tev) / KE, 3)
+                 for n, j in (("h2d_ms", 0), ("compute_ms", 2), ("d2h_ms", 4))}
         e2e = {"value": replica_value(ws, step_flops_headline, e2e_ms), "unit": "TFLOP/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "parts_mean": parts,
                "pipelined": "H2D of step i+1 and D2H of step i-1 overlap step i's kernels; "
                             "device outputs and workspaces allocated once"}
 

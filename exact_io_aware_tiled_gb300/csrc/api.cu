@@ -362,6 +362,9 @@ fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v
   a.dk = dk;
   a.dv = dv;
   a.kst = skv;
+  // 32-byte row pieces (16 columns of 16 bits) can go out as single 32-byte stores
+  a.dkv_v8 = ((reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 31u) == 0 &&
+             skv.n % 16 == 0 && skv.h % 16 == 0 && skv.b % 16 == 0;
   {
     ProfScope prof(p, st);
     e = p->d == 128 ? launch_bwd_tc128(p->dtype, mq, mk, mv, mdo, macc, a, st)

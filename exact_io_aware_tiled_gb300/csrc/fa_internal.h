@@ -87,6 +87,7 @@ struct BwdArgs {
   void* dk;                   // [B,H_kv,N,64] outputs, element strides kst
   void* dv;
   Strides kst;
+  int dkv_v8;                 // dk, dv and kst allow 32-byte stores
   int* sched;                 // work-item counter of the persistent kernel (zeroed by the prepass)
   int* status;
 };
