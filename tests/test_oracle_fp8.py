@@ -151,3 +151,28 @@ def test_block_scales_with_rotation_beat_one_scale_per_tensor_with_outliers():
     # rounded to E4M3 as well, an error both variants share
     assert e_tensor / e_block_rot > 1.3, (e_tensor, e_block_rot)
     assert e_block_rot < 0.1
+
+
+def test_probabilities_are_rounded_against_the_running_max():
+    # Row 0 sees key tile 0 with every score 0 and key tile 1 with every score
+    # equal to 3 (no rotation, equal V block scales, so c_t = 256).  Against
+    # the running max each tile's probabilities are exactly 1 when rounded,
+    # so the FP8 forward equals exact attention of the dequantised inputs;
+    # rounding against the final max would round exp(-3) * 256 inexactly.
+    N, d = 256, 64
+    q = np.zeros((1, 1, N, d), dtype=np.float32)
+    k = np.zeros((1, 1, N, d), dtype=np.float32)
+    q[0, 0, :, 0] = 24.0                  # tau * 24 * 1 = 3 with tau = 1/8
+    k[0, 0, 128:, 0] = 1.0
+    rng = np.random.default_rng(5)
+    v = rng.standard_normal((1, 1, N, d)).astype(np.float32)
+    v[0, 0, 0, 0] = v[0, 0, 128, 0] = 4.0  # both V blocks have amax 4: equal scales
+    v = np.clip(v, -3.9, 3.9)
+    v[0, 0, 0, 0] = v[0, 0, 128, 0] = 4.0
+    spec = A.Spec(B=1, H=1, N=N, d=d)
+    O, L, Al, qz = F.attention_fwd(spec, q, k, v)
+    assert qz["sv"][0, 0, 0] == qz["sv"][0, 0, 1]
+    back = {n: F.dequantize(qz[n + "8"], qz["s" + n]) for n in ("q", "k", "v")}
+    Oe, Le = A.attention_fwd(spec, back["q"], back["k"], back["v"])
+    assert np.abs(O - Oe).max() < 1e-12
+    assert np.abs(L - Le).max() < 1e-12

@@ -34,6 +34,19 @@ MUTATIONS = [
     ("attention.py", "dk[b, h // g] += r[\"dk\"]", "dk[b, h // g] = r[\"dk\"]"),
     ("attention.py", "O[b, h], L[b, h] = head_forward(spec, b, h, q[b, h], k[b, h // g], v[b, h // g])",
      "O[b, h], L[b, h] = head_forward(spec, b, h, q[b, h], k[b, h % spec.hkv], v[b, h % spec.hkv])"),
+    # the FP8 forward (oracle/fp8.py)
+    ("fp8.py", "mm = np.rint((mant * 2.0 - 1.0) * 8.0)", "mm = np.floor((mant * 2.0 - 1.0) * 8.0 + 0.5)"),
+    ("fp8.py", "code = np.minimum(code, 0x7E)", "code = np.minimum(code, 0x7F)"),
+    ("fp8.py", "sub = a < 2.0 ** -6", "sub = a < 2.0 ** -7"),
+    ("fp8.py", "return (s[:, None] * sylvester(d)) / np.sqrt(d)", "return (s[:, None] * sylvester(d)) / d"),
+    ("fp8.py", "z[..., 1, :] = a - b", "z[..., 1, :] = b - a"),
+    ("fp8.py", "scale = (amax / f448).astype(np.float32)", "scale = (amax / np.float32(240)).astype(np.float32)"),
+    ("fp8.py", "Oc = unrotate_rows(Orot, signs)", "Oc = Orot"),
+    ("fp8.py", "c = P_SCALE * sv / SV if SV > 0 else np.zeros_like(sv)", "c = P_SCALE * np.ones_like(sv)"),
+    ("fp8.py", "mrun = np.maximum.accumulate(tmax, axis=1)",
+     "mrun = np.repeat(tmax.max(axis=1, keepdims=True), nt, axis=1)"),
+    ("fp8.py", "alpha = np.where(vis, np.exp(mj - mfin_safe[:, None]), 0.0)",
+     "alpha = np.where(vis, np.exp(mfin_safe[:, None] - mj), 0.0)"),
 ]
 
 
@@ -44,13 +57,16 @@ def test_pins_catch_planted_mistake(tmp_path, fname, old, new):
     shutil.copytree(os.path.join(ROOT, "oracle"), dst / "oracle")
     shutil.copytree(os.path.join(ROOT, "tests"), dst / "tests",
                     ignore=shutil.ignore_patterns("test_oracle_mutations.py", "__pycache__", "test_gpu*", "test_zz*"))
+    # the seeded input generator (no attention arithmetic) for the FP8 pins
+    shutil.copytree(os.path.join(ROOT, "exact_io_aware_tiled_gb300"), dst / "exact_io_aware_tiled_gb300",
+                    ignore=shutil.ignore_patterns("csrc", "_build", "*.so", "__pycache__"))
     p = dst / "oracle" / fname
     src = p.read_text()
     assert src.count(old) == 1, "mutation anchor not found: " + old
     p.write_text(src.replace(old, new))
     tests = [str(dst / "tests" / t) for t in ("test_oracle_attention.py", "test_oracle_tiled.py",
                                              "test_oracle_philox.py", "test_oracle_traffic.py",
-                                             "test_oracle_gqa_window.py")]
+                                             "test_oracle_gqa_window.py", "test_oracle_fp8.py")]
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "-m", "not slow", *tests], cwd=dst, capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, "planted mistake survived every pin:\n" + r.stdout[-2000:]
