@@ -233,7 +233,7 @@ fa_status check_fp8(const fa_params* p, const fa_fp8_params* f) {
   fa_status s = check_params(p);
   if (s != FA_OK) return s;
   if (f == nullptr) return FA_ERR_INVALID_ARG;
-  if (p->dtype == FA_DT_F32 || p->d != 64 || p->dropout_p > 0.f) return FA_ERR_UNSUPPORTED;
+  if (p->dtype == FA_DT_F32 || (p->d != 64 && p->d != 128) || p->dropout_p > 0.f) return FA_ERR_UNSUPPORTED;
   if (f->per_tensor != 0 && f->per_tensor != 1) return FA_ERR_INVALID_ARG;
   if (f->signs != nullptr && !aligned16(f->signs)) return FA_ERR_MISALIGNED;
   return FA_OK;
@@ -438,6 +438,7 @@ fa_status fa_fp8_quantize(const fa_params* p, const fa_fp8_params* f, const void
   a.amax = reinterpret_cast<float*>(w + L.amax);
   a.signs = f->signs;
   a.B = p->B; a.N = p->N; a.nt = L.nt; a.npad = L.npad;
+  a.d = p->d;
   return cuda_status(launch_fp8_quantize(p->dtype, a, f->per_tensor, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -475,18 +476,21 @@ fa_status fa_fwd_fp8(const fa_params* p, const fa_fp8_params* f, const void* buf
   a.f8.o_bf16 = p->dtype == FA_DT_BF16 ? 1 : 0;
 
   const cuuint64_t N = (cuuint64_t)p->N, npad = (cuuint64_t)Q.npad, H = (cuuint64_t)p->H, Hk = (cuuint64_t)hkv;
+  const cuuint64_t d = (cuuint64_t)p->d;
+  // Q8 / K8 rows are d bytes: 64-byte swizzle for d = 64, 128-byte for d = 128
+  const CUtensorMapSwizzle swqk = p->d == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   CUtensorMap mq, mk, mv, mo;
-  if ((s = map_u8(&mq, qb + Q.q8, {64, N, H, (cuuint64_t)p->B}, {64, 64 * N, 64 * N * H}, 64, kTile,
-                  CU_TENSOR_MAP_SWIZZLE_64B)) != FA_OK ||
-      (s = map_u8(&mk, qb + Q.k8, {64, N, Hk, (cuuint64_t)p->B}, {64, 64 * N, 64 * N * Hk}, 64, kTile,
-                  CU_TENSOR_MAP_SWIZZLE_64B)) != FA_OK ||
-      (s = map_u8(&mv, qb + Q.v8t, {npad, 64, Hk, (cuuint64_t)p->B}, {npad, 64 * npad, 64 * npad * Hk}, kTile, 64,
-                  CU_TENSOR_MAP_SWIZZLE_128B)) != FA_OK ||
+  if ((s = map_u8(&mq, qb + Q.q8, {d, N, H, (cuuint64_t)p->B}, {d, d * N, d * N * H}, (cuuint32_t)d, kTile, swqk)) !=
+          FA_OK ||
+      (s = map_u8(&mk, qb + Q.k8, {d, N, Hk, (cuuint64_t)p->B}, {d, d * N, d * N * Hk}, (cuuint32_t)d, kTile, swqk)) !=
+          FA_OK ||
+      (s = map_u8(&mv, qb + Q.v8t, {npad, d, Hk, (cuuint64_t)p->B}, {npad, d * npad, d * npad * Hk}, kTile,
+                  (cuuint32_t)d, CU_TENSOR_MAP_SWIZZLE_128B)) != FA_OK ||
       (s = map16(&mo, o, p, p->H, strides_of(p))) != FA_OK)
     return s;
   if ((s = prepare_common(p, L, w, st)) != FA_OK) return s;
   ProfScope prof(p, st);
-  return cuda_status(launch_fwd_fp8(mq, mk, mv, mo, a, st));
+  return cuda_status(launch_fwd_fp8(p->d, mq, mk, mv, mo, a, st));
 }
 
 const char* fa_status_string(fa_status s) {

@@ -40,7 +40,7 @@ struct Fp8Args {
   const float* sq;            // [B*H][nt]: dequantisation scale of each 128-row Q tile
   const float* sk;            // [B*H_kv][nt]
   const float* sv;            // [B*H_kv][nt]
-  const int8_t* signs;        // [64] signs of the rotation, or nullptr (no rotation)
+  const int8_t* signs;        // [d] signs of the rotation, or nullptr (no rotation)
   int nt;                     // tiles per head, ceil(N / 128)
   int o_bf16;                 // O is stored as bfloat16 (else float16)
 };
@@ -62,14 +62,15 @@ struct FwdArgs {
 // Quantiser of the FP8 forward: Q, K and V rows (optionally rotated) to E4M3
 // with one scale per 128-row tile (or per tensor).
 struct Fp8QuantArgs {
-  const void* src[3];         // Q [B,H,N,64], K and V [B,H_kv,N,64], 16-bit
+  const void* src[3];         // Q [B,H,N,d], K and V [B,H_kv,N,d], 16-bit
   Strides st[3];              // element strides of each source
   int heads[3];               // H, H_kv, H_kv
-  uint8_t* dst[3];            // Q8 [B,H,N,64], K8 [B,H_kv,N,64], V8^T [B,H_kv,64,npad]
+  uint8_t* dst[3];            // Q8 [B,H,N,d], K8 [B,H_kv,N,d], V8^T [B,H_kv,d,npad]
   float* scale[3];            // [B*heads][nt]
   float* amax;                // [3] per-tensor maxima (scratch of the per-tensor mode)
-  const int8_t* signs;        // [64] or nullptr
+  const int8_t* signs;        // [d] or nullptr
   int B, N, nt, npad;
+  int d;                      // head dimension, 64 or 128
 };
 
 struct BwdArgs {
@@ -124,9 +125,9 @@ cudaError_t launch_block_lists(const uint8_t* mask, int nb, int16_t* row_list, i
 cudaError_t launch_dropout_mask(const DropoutArgs& d, int H, int N, int b, int h, int row0, int nrows,
                                 uint8_t* out, cudaStream_t s);
 // FP8 forward: quantise Q, K, V (per_tensor selects one scale per tensor),
-// then the attention forward on the quantised operands (head dimension 64).
+// then the attention forward on the quantised operands (head dimension d = 64 or 128).
 cudaError_t launch_fp8_quantize(int dtype, const Fp8QuantArgs& a, int per_tensor, cudaStream_t s);
-cudaError_t launch_fwd_fp8(const CUtensorMap& q8, const CUtensorMap& k8, const CUtensorMap& v8t,
+cudaError_t launch_fwd_fp8(int d, const CUtensorMap& q8, const CUtensorMap& k8, const CUtensorMap& v8t,
                            const CUtensorMap& o, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_wait_selftest(int* status, int* out, unsigned long long* out_ns, cudaStream_t s);
 

@@ -9,23 +9,25 @@
 // Readings fixed here (the pages leave them open):
 //   * the format is E4M3 (largest finite 448), rounded to nearest even and
 //     saturated;
-//   * the rotation is M = diag(s) H_64 / 8 with s the caller's random signs;
+//   * the rotation is M = diag(s) H_D / sqrt(D) with s the caller's random
+//     signs (D = 64 or 128);
 //     Q, K and V rows are all rotated (the scores are unchanged because M is
 //     orthogonal; the forward rotates O back);
-//   * a block is 128 rows x 64 of one head; its scale is amax / 448 and its
+//   * a block is 128 rows x D of one head; its scale is amax / 448 and its
 //     codes are E4M3(x * (448 / amax)); an all-zero block has scale 0;
 //   * the per-tensor variant (the pages' baseline) uses the amax of the
 //     whole tensor for every block.
 // The codes are integers decided by float32 arithmetic, so the order is
-// fixed: sign flip, butterflies (stage h = 1, 2, ..., 32), multiply by 1/8,
+// fixed: sign flip, butterflies (stage h = 1, 2, ..., D/2), multiply by the
+// float32 value of 1/sqrt(D) (1/8 exactly for D = 64),
 // amax, inv = 448 / amax (correctly rounded), x * inv, E4M3 rounding.
 //
 // One CTA of 128 threads per block; thread r owns row r.  The block's rows
 // are loaded and stored cooperatively (consecutive threads move consecutive
 // 16-byte chunks) through shared memory, whose 16-byte chunks are XOR-
 // swizzled with the row so that the per-row accesses are free of bank
-// conflicts.  Q and K codes are written row-major ([B, heads, N, 64] bytes);
-// V codes are written transposed ([B, H_kv, 64, npad] bytes, keys
+// conflicts.  Q and K codes are written row-major ([B, heads, N, D] bytes);
+// V codes are written transposed ([B, H_kv, D, npad] bytes, keys
 // contiguous, zero past N) so that the P V product reads both of its
 // operands K-major.
 #include "fp8.cuh"
@@ -36,12 +38,26 @@ namespace {
 constexpr float kE4M3Max = 448.f;
 enum QuantMode { kPerBlock = 0, kAmaxOnly = 1, kPerTensor = 2 };
 
-template <typename T, int kMode>
+// 16-byte chunk position of code chunk k of row q in the staging tile (rows
+// of D bytes): XOR-swizzled so that a warp's per-row accesses spread over
+// all banks
+template <int D> __device__ __forceinline__ int swz_code(int k, int q) {
+  return D == 64 ? ((k ^ (q >> 1)) & 3) : ((k ^ q) & 7);
+}
+
+// float32 value of 1 / sqrt(D): 1/8 exactly, or the rounded 1/sqrt(128)
+template <int D> __device__ __forceinline__ float inv_sqrt_d() {
+  return D == 64 ? 0.125f : __int_as_float(0x3db504f3);
+}
+
+template <typename T, int D, int kMode>
 __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
+  constexpr int RB = D * 2;          // bytes of a 16-bit row
+  constexpr int CH = RB / 16;        // its 16-byte chunks
   __shared__ float red[4];
-  // the block's 16-bit rows (128 x 128 bytes), later its codes: Q / K rows
-  // (128 x 64 bytes) or the transposed V codes (64 x 128 bytes)
-  __shared__ __align__(128) uint8_t tile[kTile * 128];
+  // the block's 16-bit rows (128 x RB bytes), later its codes: Q / K rows
+  // (128 x D bytes) or the transposed V codes (D x 128 bytes)
+  __shared__ __align__(128) uint8_t tile[kTile * RB];
 
   // tensor x and block (b, head, tile) of this CTA
   int blk = (int)blockIdx.x;
@@ -63,21 +79,21 @@ __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
   const int n = t * kTile + r;
   const Strides st = a.st[x];
 
-  // cooperative load: chunk k (16 bytes) of row q goes to q * 128 + ((k ^ q) & 7) * 16
+  // cooperative load: chunk k (16 bytes) of row q goes to q * RB + (k ^ (q & 7)) * 16
   const T* base = static_cast<const T*>(a.src[x]) + b * st.b + h * st.h;
   const int rows = min(kTile, a.N - t * kTile);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int idx = r + i * kTile, q = idx >> 3, k = idx & 7;
+  for (int i = 0; i < CH; ++i) {
+    const int idx = r + i * kTile, q = idx / CH, k = idx % CH;
     uint4 u = make_uint4(0u, 0u, 0u, 0u);
     if (q < rows) u = *reinterpret_cast<const uint4*>(base + (int64_t)(t * kTile + q) * st.n + k * 8);
-    *reinterpret_cast<uint4*>(tile + q * 128 + (((k ^ q) & 7) << 4)) = u;
+    *reinterpret_cast<uint4*>(tile + q * RB + ((k ^ (q & 7)) << 4)) = u;
   }
   __syncthreads();
-  float v[64];
+  float v[D];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint4 u = *reinterpret_cast<const uint4*>(tile + r * 128 + (((j ^ r) & 7) << 4));
+  for (int j = 0; j < CH; ++j) {
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + r * RB + ((j ^ (r & 7)) << 4));
     const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -88,7 +104,7 @@ __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
   if (a.signs != nullptr) {
     const uint4* sp = reinterpret_cast<const uint4*>(a.signs);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < D / 16; ++j) {
       const uint4 u = sp[j];
       const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -97,15 +113,16 @@ __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
         if (sg < 0) v[16 * j + c] = -v[16 * j + c];
       }
     }
-    fwht_rows<64>(v);
+    fwht_rows<D>(v);
+    const float sc = inv_sqrt_d<D>();
 #pragma unroll
-    for (int c = 0; c < 64; ++c) v[c] = __fmul_rn(v[c], 0.125f);
+    for (int c = 0; c < D; ++c) v[c] = __fmul_rn(v[c], sc);
   }
 
   // block amax
   float am = 0.f;
 #pragma unroll
-  for (int c = 0; c < 64; ++c) am = fmaxf(am, fabsf(v[c]));
+  for (int c = 0; c < D; ++c) am = fmaxf(am, fabsf(v[c]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
   if ((r & 31) == 0) red[r >> 5] = am;
@@ -121,42 +138,45 @@ __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
   if constexpr (kMode == kPerTensor) am = a.amax[x];
   if (r == 0) *sc = __fdiv_rn(am, kE4M3Max);
   const float inv = am > 0.f ? __fdiv_rn(kE4M3Max, am) : 0.f;
-  uint32_t w[16];
+  uint32_t w[D / 4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
+  for (int j = 0; j < D / 4; ++j)
     w[j] = e4m3x4(__fmul_rn(v[4 * j], inv), __fmul_rn(v[4 * j + 1], inv), __fmul_rn(v[4 * j + 2], inv),
                   __fmul_rn(v[4 * j + 3], inv));
 
   if (x < 2) {
-    // codes of row r to r * 64 + ((j ^ (r >> 1)) & 3) * 16, then cooperative stores
+    // codes of row r (D bytes, D / 16 chunks) to swizzled chunk positions,
+    // then cooperative stores
+    constexpr int CC = D / 16;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      *reinterpret_cast<uint4*>(tile + r * 64 + (((j ^ (r >> 1)) & 3) << 4)) =
+    for (int j = 0; j < CC; ++j)
+      *reinterpret_cast<uint4*>(tile + r * D + (swz_code<D>(j, r) << 4)) =
           make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
     __syncthreads();
-    uint8_t* dst = a.dst[x] + ((size_t)bh * a.N + (size_t)t * kTile) * 64;
+    uint8_t* dst = a.dst[x] + ((size_t)bh * a.N + (size_t)t * kTile) * D;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int idx = r + i * kTile, q = idx >> 2, k = idx & 3;
+    for (int i = 0; i < CC; ++i) {
+      const int idx = r + i * kTile, q = idx / CC, k = idx % CC;
       if (q < rows)
-        *reinterpret_cast<uint4*>(dst + q * 64 + k * 16) =
-            *reinterpret_cast<const uint4*>(tile + q * 64 + (((k ^ (q >> 1)) & 3) << 4));
+        *reinterpret_cast<uint4*>(dst + q * D + k * 16) =
+            *reinterpret_cast<const uint4*>(tile + q * D + (swz_code<D>(k, q) << 4));
     }
   } else {
     // transpose through shared memory: vt[c][r] = code c of row r.  Keys past
     // N get the code 0 (the rotated zero row can hold -0, code 0x80).
     if (n >= a.N) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) w[j] = 0u;
+      for (int j = 0; j < D / 4; ++j) w[j] = 0u;
     }
 #pragma unroll
-    for (int c = 0; c < 64; ++c) tile[c * kTile + r] = (uint8_t)((w[c >> 2] >> ((c & 3) * 8)) & 0xFFu);
+    for (int c = 0; c < D; ++c) tile[c * kTile + r] = (uint8_t)((w[c >> 2] >> ((c & 3) * 8)) & 0xFFu);
     __syncthreads();
-    const int c = r >> 1, half = r & 1;
-    const uint4* src = reinterpret_cast<const uint4*>(tile + c * kTile + half * 64);
-    uint4* dst = reinterpret_cast<uint4*>(a.dst[2] + ((size_t)bh * 64 + c) * a.npad + t * kTile + half * 64);
+    // D rows of 128 bytes: thread r writes D bytes of row r * D / 128
+    const int c = (r * D) / kTile, off = (r * D) % kTile;
+    const uint4* src = reinterpret_cast<const uint4*>(tile + c * kTile + off);
+    uint4* dst = reinterpret_cast<uint4*>(a.dst[2] + ((size_t)bh * D + c) * a.npad + t * kTile + off);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) dst[j] = src[j];
+    for (int j = 0; j < D / 16; ++j) dst[j] = src[j];
   }
 }
 
@@ -178,28 +198,30 @@ __global__ void __launch_bounds__(256) fp8_amax_reduce_kernel(const Fp8QuantArgs
   }
 }
 
-template <typename T>
+template <typename T, int D>
 cudaError_t launch_t(const Fp8QuantArgs& a, int per_tensor, cudaStream_t s) {
   const long long nblk = (long long)a.B * (a.heads[0] + a.heads[1] + a.heads[2]) * a.nt;
   if (nblk <= 0) return cudaSuccess;
   if (nblk >= (1ll << 31)) return cudaErrorInvalidValue;
   if (!per_tensor) {
-    fp8_quant_kernel<T, kPerBlock><<<(unsigned)nblk, 128, 0, s>>>(a);
+    fp8_quant_kernel<T, D, kPerBlock><<<(unsigned)nblk, 128, 0, s>>>(a);
     return cudaGetLastError();
   }
-  fp8_quant_kernel<T, kAmaxOnly><<<(unsigned)nblk, 128, 0, s>>>(a);
+  fp8_quant_kernel<T, D, kAmaxOnly><<<(unsigned)nblk, 128, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   fp8_amax_reduce_kernel<<<3, 256, 0, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  fp8_quant_kernel<T, kPerTensor><<<(unsigned)nblk, 128, 0, s>>>(a);
+  fp8_quant_kernel<T, D, kPerTensor><<<(unsigned)nblk, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fp8_quantize(int dtype, const Fp8QuantArgs& a, int per_tensor, cudaStream_t s) {
-  return dtype == FA_DT_BF16 ? launch_t<__nv_bfloat16>(a, per_tensor, s) : launch_t<__half>(a, per_tensor, s);
+  if (a.d == 128)
+    return dtype == FA_DT_BF16 ? launch_t<__nv_bfloat16, 128>(a, per_tensor, s) : launch_t<__half, 128>(a, per_tensor, s);
+  return dtype == FA_DT_BF16 ? launch_t<__nv_bfloat16, 64>(a, per_tensor, s) : launch_t<__half, 64>(a, per_tensor, s);
 }
 
 }  // namespace fa

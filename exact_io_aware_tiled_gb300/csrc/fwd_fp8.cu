@@ -1,4 +1,4 @@
-// fwd_fp8.cu -- FP8 (E4M3) attention forward on sm_103a, head dimension 64.
+// fwd_fp8.cu -- FP8 (E4M3) attention forward on sm_103a, head dimension 64 or 128.
 //
 // Method: the Q-outer online-softmax forward of fwd_tc.cu (lynx-cortex, "El
 // algoritmo Flash (forward)"; marketmaker.cc, "O algoritmo de atencao do
@@ -8,8 +8,8 @@
 // marketmaker.cc, "FA3: Mecanica da tremonha", item 3).  Both products run
 // on the tensor cores in E4M3 (tcgen05.mma kind::f8f6f4):
 //
-//   S   = Q8 K8^T                  M = 128, N = 128, K = 64   (2 MMAs of K 32)
-//   O' += A V8 (A = P8, V8^T)      M = 128, N = 64,  K = 128  (4 MMAs of K 32)
+//   S   = Q8 K8^T                  M = 128, N = 128, K = D    (D / 32 MMAs of K 32)
+//   O' += A V8 (A = P8, V8^T)      M = 128, N = D,   K = 128  (4 MMAs of K 32)
 //
 // Scales: the scores of query tile i and key tile t are
 // tau * sq_i * sk_t * (Q8 K8^T), folded into the softmax's exponent
@@ -19,15 +19,16 @@
 // V scale; m is the running row max, moved (and O rescaled) whenever it
 // grows, so exp(S - m) <= 1 and A <= 256 < 448.  The row sum l uses the
 // unrounded probabilities.  At the end O' = (SV / 256) acc / l is rotated
-// back, O = (O' H_64) o s / 8, and stored in the input's 16-bit type.
+// back, O = (O' H_D) o s / sqrt(D), and stored in the input's 16-bit type.
 //
 // GB300 mapping: as fwd_tc.cu -- one CTA holds two 128-row query tiles of
-// one head; warp 8 streams K8 / V8^T tiles (8 KB each) with TMA into a ring;
+// one head; warp 8 streams K8 / V8^T tiles (D x 128 bytes each) with TMA into a ring;
 // warp 9 issues S for both slots; warps 10 / 11 issue the P V products; warps
 // 0-3 / 4-7 are the softmax of slot 0 / 1, one thread per row.  The E4M3
 // probabilities go to shared memory (128-byte swizzle, K-major), not to
 // tensor memory, so both operands of the second product come from shared
-// memory.  Tensor memory per slot: S 128 columns | O 64.
+// memory.  Tensor memory per slot: S 128 columns | O D.  Q8 / K8 rows are
+// D bytes: 64-byte swizzle for D = 64, 128-byte swizzle for D = 128.
 #include "common.cuh"
 #include "fp8.cuh"
 #include "fwd_plan.cuh"
@@ -39,11 +40,12 @@ constexpr int kThreads = 384;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kPScale = 256.f;
 
+template <int D>
 struct Fp8Cfg {
-  static constexpr int kQT = kTile * 64;       // Q8 / K8 tile: 128 rows x 64 bytes (64-byte swizzle)
-  static constexpr int kVT = 64 * kTile;       // V8^T tile: 64 rows x 128 bytes (128-byte swizzle)
-  static constexpr int kPT = kTile * kTile;    // P8 tile: 128 rows x 128 bytes; also O's staging tile
-  static constexpr int NS = 6;                 // K/V stages
+  static constexpr int kQT = kTile * D;        // Q8 / K8 tile: 128 rows x D bytes
+  static constexpr int kVT = D * kTile;        // V8^T tile: D rows x 128 bytes (128-byte swizzle)
+  static constexpr int kPT = kTile * kTile;    // P8 tile: 128 rows x 128 bytes; also a staging box of O
+  static constexpr int NS = D == 64 ? 6 : 4;   // K/V stages
   static constexpr int kQ = 0;                 // 2 Q tiles
   static constexpr int kK = 2 * kQT;           // NS K tiles
   static constexpr int kV = kK + NS * kQT;     // NS V tiles
@@ -53,30 +55,39 @@ struct Fp8Cfg {
   static constexpr int kBytes = kBar + 512;
   static constexpr int kDyn = kBytes + 1024;   // + alignment slack
 };
-static_assert(Fp8Cfg::kDyn <= 232448, "shared memory over the per-block limit");
-static_assert(Fp8Cfg::kK % 1024 == 0 && Fp8Cfg::kV % 1024 == 0 && Fp8Cfg::kP % 1024 == 0, "tiles are 1024-B aligned");
+static_assert(Fp8Cfg<64>::kDyn <= 232448 && Fp8Cfg<128>::kDyn <= 232448, "shared memory over the per-block limit");
+static_assert(Fp8Cfg<128>::kK % 1024 == 0 && Fp8Cfg<128>::kV % 1024 == 0 && Fp8Cfg<128>::kP % 1024 == 0 &&
+              Fp8Cfg<64>::kK % 1024 == 0 && Fp8Cfg<64>::kV % 1024 == 0 && Fp8Cfg<64>::kP % 1024 == 0,
+              "tiles are 1024-B aligned");
 
+template <int NS>
 struct Fp8Bars {
   uint64_t q_full;
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t done[3];
-  uint64_t k_full[Fp8Cfg::NS], v_full[Fp8Cfg::NS], k_empty[Fp8Cfg::NS], v_empty[Fp8Cfg::NS];
+  uint64_t k_full[NS], v_full[NS], k_empty[NS], v_empty[NS];
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(Fp8Bars) <= 512, "barrier block overflows its shared-memory slot");
+static_assert(sizeof(Fp8Bars<6>) <= 512, "barrier block overflows its shared-memory slot");
 
-template <bool kWin>
+// Shared-memory descriptor of a Q8 / K8 tile (rows of D bytes, K-major).
+template <int D>
+__device__ __forceinline__ uint64_t qk_desc(uint32_t saddr) {
+  return D == 64 ? sdesc_sw64(saddr, 512) : sdesc_sw128(saddr, 16, 1024);
+}
+
+template <int D, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                const FwdArgs a) {
-  using C = Fp8Cfg;
+  using C = Fp8Cfg<D>;
   constexpr int NS = C::NS;
   constexpr uint32_t kColO = 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Fp8Bars* bars = reinterpret_cast<Fp8Bars*>(smem + C::kBar);
+  Fp8Bars<NS>* bars = reinterpret_cast<Fp8Bars<NS>*>(smem + C::kBar);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -166,9 +177,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     // ===================== S issuer (both slots) =====================
     if (lane == 0 && smax > 0) {
       constexpr uint32_t idS = idesc_e4m3(128, 128);
-      const uint64_t qd[2] = {sdesc_sw64(smem_u32(smem + C::kQ), 512),
-                              sdesc_sw64(smem_u32(smem + C::kQ + C::kQT), 512)};
-      const uint64_t kd0 = sdesc_sw64(smem_u32(smem + C::kK), 512);
+      const uint64_t qd[2] = {qk_desc<D>(smem_u32(smem + C::kQ)), qk_desc<D>(smem_u32(smem + C::kQ + C::kQT))};
+      const uint64_t kd0 = qk_desc<D>(smem_u32(smem + C::kK));
       bool ok = mbar_wait(&bars->q_full, 0, ctl);
       int ld = 0;
       for (int s = 0; s < smax && ok; ++s) {
@@ -183,9 +193,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           tc_fence_after();
           const uint64_t kd = kd0 + (uint64_t)((p.stage(l) * C::kQT) >> 4);
           const uint32_t tS = tmem + x * 256;
-          // K-dim = 64 bytes in two steps of 32 within the 64-byte rows
+          // K-dim = D bytes in steps of 32 within the D-byte rows
 #pragma unroll
-          for (int k = 0; k < 2; ++k) mma_ss_e4m3(tS, qd[x] + 2 * k, kd + 2 * k, idS, k > 0 ? 1u : 0u);
+          for (int k = 0; k < D / 32; ++k) mma_ss_e4m3(tS, qd[x] + 2 * k, kd + 2 * k, idS, k > 0 ? 1u : 0u);
           mma_commit(&bars->s_full[x]);
         }
 #pragma unroll
@@ -199,7 +209,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     // ===================== P V issuer of slot x =====================
     const int x = warp - 10;
     if (lane == 0 && smax > 0) {
-      constexpr uint32_t idPV = idesc_e4m3(128, 64);
+      constexpr uint32_t idPV = idesc_e4m3(128, D);
       const uint64_t pd = sdesc_sw128(smem_u32(smem + C::kP + x * C::kPT), 16, 1024);
       const uint64_t vd0 = sdesc_sw128(smem_u32(smem + C::kV), 16, 1024);
       const uint32_t tO = tmem + x * 256 + kColO;
@@ -351,7 +361,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       // any of its rows needs it (alpha is exactly 1 for the other rows)
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = 0; hf < D / 32; ++hf) {
           uint32_t o[32];
           tmem_ld32(tO + hf * 32, o);
           tmem_wait_ld();
@@ -373,60 +383,70 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       const float post = l_run > 0.f ? (SV / kPScale) / l_run : 0.f;
       const bool row_ok = i < a.N && S.qt < a.nq;
       const size_t row = (size_t)(b * a.H + h) * a.N + i;
-      float o[64];
+      float o[D];
       if (have) {
-        uint32_t raw[2][32];
-        tmem_ld32(tO, raw[0]);
-        tmem_ld32(tO + 32, raw[1]);
-        tmem_wait_ld();
-        reg_fence32(raw[0]);
-        reg_fence32(raw[1]);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) o[c] = __uint_as_float(raw[c >> 5][c & 31]) * post;
+        for (int hf = 0; hf < D / 64; ++hf) {
+          uint32_t raw[2][32];
+          tmem_ld32(tO + hf * 64, raw[0]);
+          tmem_ld32(tO + hf * 64 + 32, raw[1]);
+          tmem_wait_ld();
+          reg_fence32(raw[0]);
+          reg_fence32(raw[1]);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) o[hf * 64 + c] = __uint_as_float(raw[c >> 5][c & 31]) * post;
+        }
       } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) o[c] = 0.f;
+        for (int c = 0; c < D; ++c) o[c] = 0.f;
       }
       if (a.f8.signs != nullptr) {
-        // O = O' M^T = (O' H) o s / 8
-        fwht_rows<64>(o);
+        // O = O' M^T = (O' H) o s / sqrt(D)
+        fwht_rows<D>(o);
+        const float sc = D == 64 ? 0.125f : __int_as_float(0x3db504f3);
         const uint4* sp = reinterpret_cast<const uint4*>(a.f8.signs);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < D / 16; ++j) {
           const uint4 u = sp[j];
           const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int8_t sg = (int8_t)((w4[c >> 2] >> ((c & 3) * 8)) & 0xFFu);
-            o[16 * j + c] *= (sg < 0 ? -0.125f : 0.125f);
+            o[16 * j + c] *= (sg < 0 ? -sc : sc);
           }
         }
       }
-      // the slot's P tile is free once its last P V product is done
-      uint8_t* ob = pt;
+      // 64-column boxes of O staged in the slot's P tile (free once its last
+      // P V product is done) and, for D = 128, its Q tile (free once its last S is)
+      uint8_t* obox[2] = {pt, smem + C::kQ + x * C::kQT};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t w[4];
-        if (a.f8.o_bf16) {
+      for (int hh = 0; hh < D / 64; ++hh) {
 #pragma unroll
-          for (int t = 0; t < 4; ++t) w[t] = Cvt<__nv_bfloat16>::pack(o[j * 8 + 2 * t], o[j * 8 + 2 * t + 1]);
-        } else {
+        for (int j = 0; j < 8; ++j) {
+          uint32_t w[4];
+          const int c0 = hh * 64 + j * 8;
+          if (a.f8.o_bf16) {
 #pragma unroll
-          for (int t = 0; t < 4; ++t) w[t] = Cvt<__half>::pack(o[j * 8 + 2 * t], o[j * 8 + 2 * t + 1]);
+            for (int t = 0; t < 4; ++t) w[t] = Cvt<__nv_bfloat16>::pack(o[c0 + 2 * t], o[c0 + 2 * t + 1]);
+          } else {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) w[t] = Cvt<__half>::pack(o[c0 + 2 * t], o[c0 + 2 * t + 1]);
+          }
+          const uint32_t off = r * 128 + (((j ^ r) & 7) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                       :: "r"(smem_u32(obox[hh] + off)), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
         }
-        const uint32_t off = r * 128 + (((j ^ r) & 7) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                     :: "r"(smem_u32(ob + off)), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
       }
       if (row_ok && a.o_f32 != nullptr) {
-        float4* dst = reinterpret_cast<float4*>(a.o_f32 + row * 64);
+        float4* dst = reinterpret_cast<float4*>(a.o_f32 + row * D);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) dst[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
       }
       fence_proxy_async_smem();
       named_bar_sync(1 + x, 128);
       if (r == 0 && S.qt < a.nq) {
-        tma_store_4d(&tmO, ob, 0, S.qt * kTile, h, b);
+#pragma unroll
+        for (int hh = 0; hh < D / 64; ++hh) tma_store_4d(&tmO, obox[hh], hh * 64, S.qt * kTile, h, b);
         bulk_commit();
         bulk_wait_read0();
       }
@@ -442,23 +462,25 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   }
 }
 
-template <bool kWin>
+template <int D, bool kWin>
 cudaError_t launch_w(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
                      const FwdArgs& a, cudaStream_t s) {
-  auto kern = fwd_fp8_kernel<kWin>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Fp8Cfg::kDyn);
+  auto kern = fwd_fp8_kernel<D, kWin>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Fp8Cfg<D>::kDyn);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(a.npairs * a.B * a.H);
   if (grid == 0) return cudaSuccess;
-  kern<<<grid, kThreads, Fp8Cfg::kDyn, s>>>(q, k, v, o, a);
+  kern<<<grid, kThreads, Fp8Cfg<D>::kDyn, s>>>(q, k, v, o, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_fp8(const CUtensorMap& q8, const CUtensorMap& k8, const CUtensorMap& v8t,
+cudaError_t launch_fwd_fp8(int d, const CUtensorMap& q8, const CUtensorMap& k8, const CUtensorMap& v8t,
                            const CUtensorMap& o, const FwdArgs& a, cudaStream_t s) {
-  return a.mask.window > 0 ? launch_w<true>(q8, k8, v8t, o, a, s) : launch_w<false>(q8, k8, v8t, o, a, s);
+  if (d == 128)
+    return a.mask.window > 0 ? launch_w<128, true>(q8, k8, v8t, o, a, s) : launch_w<128, false>(q8, k8, v8t, o, a, s);
+  return a.mask.window > 0 ? launch_w<64, true>(q8, k8, v8t, o, a, s) : launch_w<64, false>(q8, k8, v8t, o, a, s);
 }
 
 }  // namespace fa

@@ -157,6 +157,9 @@ CONFIGS = {
     # after the random rotation
     "gpt2_medium_causal_fp8": Workload("gpt2_medium_causal_fp8", B=64, H=16, N=1024, dtype="bf16",
                                        causal=True, seed=20269),
+    # the FP8 forward at head dimension 128 (GPT-2-medium width: 8 heads of 128)
+    "gpt2_medium_d128_causal_fp8": Workload("gpt2_medium_d128_causal_fp8", B=64, H=8, N=1024, d=128,
+                                            dtype="bf16", causal=True, seed=20271),
     # FP8 error study: N(0, 1) plus 0.1 % outliers of standard deviation 10
     "outliers_fp8": Workload("outliers_fp8", B=1, H=4, N=2048, dtype="bf16", seed=20270,
                              outlier_rate=1e-3, outlier_sd=10.0),

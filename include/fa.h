@@ -241,7 +241,7 @@ fa_status fa_selftest_wait_timeout(void *ws, int32_t *out, uint64_t *out_ns, voi
  *     with m the running row max (the accumulator is rescaled whenever m
  *     grows), sv_t the V scale of tile t and SV the largest V scale of the
  *     head; the row sum uses the unrounded probabilities;
- *   - head dimension 64, float16 or bfloat16 inputs and output; causal,
+ *   - head dimension 64 or 128, float16 or bfloat16 inputs and output; causal,
  *     key padding, block-sparse masks, the sliding window and grouped K/V
  *     heads as in fa_fwd; dropout returns FA_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------- */

@@ -189,7 +189,7 @@ def test_fp8_buffer_layout(lib):
 
 @pytest.mark.parametrize("mut,fmut,code", [
     (dict(dtype=0), {}, 2),           # no float32 FP8 path
-    (dict(d=128, stride_n=128, stride_h=200 * 128, stride_b=600 * 128), {}, 2),   # head dimension 64 only
+    (dict(d=96, stride_n=96, stride_h=200 * 96, stride_b=600 * 96), {}, 2),   # head dimensions 64 and 128 only
     (dict(dropout_p=0.1), {}, 2),     # no dropout in the FP8 forward
     ({}, dict(per_tensor=2), 1),
     ({}, dict(signs=(1 << 20) + 4), 3),

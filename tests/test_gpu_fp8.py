@@ -107,6 +107,11 @@ CASES = {
                            seed=803),
     "gqa_sparse": dict(B=1, H=4, H_kv=2, N=640, dtype="bf16", sparse_butterfly=True, seed=804),
     "single_tile": dict(B=1, H=1, N=64, dtype="bf16", causal=True, seed=805),
+    # head dimension 128 (FlashAttention-3's FP8 setting)
+    "d128_causal_bf16": dict(B=1, H=2, N=300, d=128, dtype="bf16", causal=True, seed=808),
+    "d128_gqa_padding_f16": dict(B=2, H=4, H_kv=2, N=400, d=128, dtype="f16", seqlen_range=(150, 400), seed=809),
+    "d128_window_sparse": dict(B=1, H=2, N=520, d=128, dtype="bf16", causal=True, window=300,
+                               sparse_butterfly=True, seed=810),
 }
 
 
@@ -115,7 +120,7 @@ CASES = {
 def test_fp8_forward_matches_oracle(name, rotate):
     wl = W.Workload(name, **CASES[name])
     inp = W.make_inputs(wl, grads=False)
-    signs = W.rotation_signs(64, wl.seed) if rotate else None
+    signs = W.rotation_signs(wl.d, wl.seed) if rotate else None
     got = run_fp8(wl, inp, signs)
     qz = oracle_quantized(inp, signs)
     assert_codes_equal(got, qz)
@@ -187,12 +192,25 @@ def test_fp8_gpt2_medium_causal_sampled():
         check_fp8_head(wl, got, qz, b, h, signs, rows=rows, qb=(b, h, h))
 
 
+@pytest.mark.parametrize("name", ["gpt2_medium_d128_causal_fp8"])
+def test_fp8_d128_full_size_sampled(name):
+    wl = W.CONFIGS[name]
+    inp = W.make_inputs(wl, grads=False)
+    signs = W.rotation_signs(wl.d, wl.seed)
+    got = run_fp8(wl, inp, signs)
+    rows = sample_rows(wl.N, seed=9, extra=64)
+    for b, h in ((0, 0), (wl.B - 1, wl.H - 1), (33, 3)):
+        qz = oracle_quantized(inp, signs, heads=(b, h))
+        assert_codes_equal(got, qz, b=b, h=h, hk=h)
+        check_fp8_head(wl, got, qz, b, h, signs, rows=rows, qb=(b, h, h))
+
+
 def test_fp8_refuses_float32_and_other_head_dims():
     q = torch.zeros((1, 1, 128, 64), device="cuda", dtype=torch.float32)
     with pytest.raises(fa.FAError) as e:
         fa.fwd_fp8(q, q, q)
     assert e.value.code == 2
-    q = torch.zeros((1, 1, 128, 128), device="cuda", dtype=torch.bfloat16)
+    q = torch.zeros((1, 1, 128, 96), device="cuda", dtype=torch.bfloat16)
     with pytest.raises(fa.FAError) as e:
         fa.fwd_fp8(q, q, q)
     assert e.value.code == 2
