@@ -26,20 +26,40 @@ __device__ __forceinline__ uint32_t e4m3x4(float x0, float x1, float x2, float x
   return e4m3x2(x0, x1) | (e4m3x2(x2, x3) << 16);
 }
 
-// x <- x H_D (Sylvester order), in place, float32 adds and subtracts.
+// x <- x H_D (Sylvester order), in place, float32 adds and subtracts.  From
+// stage h = 2 on, the butterflies of i and i + 1 (both with bit h clear) run
+// as one packed f32x2 add and one packed subtract; each lane rounds exactly
+// as the scalar operation would, so the result is bit for bit the same.
 template <int D>
 __device__ __forceinline__ void fwht_rows(float (&x)[D]) {
 #pragma unroll
-  for (int h = 1; h < D; h <<= 1) {
+  for (int i = 0; i < D; i += 2) {
+    const float a = x[i], b = x[i + 1];
+    x[i] = __fadd_rn(a, b);
+    x[i + 1] = __fsub_rn(a, b);
+  }
 #pragma unroll
-    for (int i = 0; i < D; ++i) {
+  for (int h = 2; h < D; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < D; i += 2) {
       if ((i & h) == 0) {
-        const float a = x[i], b = x[i + h];
-        x[i] = __fadd_rn(a, b);
-        x[i + h] = __fsub_rn(a, b);
+        float s0 = x[i], s1 = x[i + 1], d0, d1;
+        sub2(d0, d1, s0, s1, x[i + h], x[i + h + 1]);
+        add2(s0, s1, x[i + h], x[i + h + 1]);
+        x[i] = s0;
+        x[i + 1] = s1;
+        x[i + h] = d0;
+        x[i + h + 1] = d1;
       }
     }
   }
+}
+
+// x[c] <- x[c] * k, packed in pairs (one rounding per lane, as scalar).
+template <int D>
+__device__ __forceinline__ void scale_rows(float (&x)[D], float k) {
+#pragma unroll
+  for (int c = 0; c < D; c += 2) mul2(x[c], x[c + 1], x[c], x[c + 1], k, k);
 }
 
 // Shared-memory matrix descriptor, 64-byte swizzle (swizzle mode 4 in bits

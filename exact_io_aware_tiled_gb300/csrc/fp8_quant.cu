@@ -114,9 +114,7 @@ __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
       }
     }
     fwht_rows<D>(v);
-    const float sc = inv_sqrt_d<D>();
-#pragma unroll
-    for (int c = 0; c < D; ++c) v[c] = __fmul_rn(v[c], sc);
+    scale_rows<D>(v, inv_sqrt_d<D>());
   }
 
   // block amax
@@ -138,11 +136,10 @@ __global__ void __launch_bounds__(128) fp8_quant_kernel(const Fp8QuantArgs a) {
   if constexpr (kMode == kPerTensor) am = a.amax[x];
   if (r == 0) *sc = __fdiv_rn(am, kE4M3Max);
   const float inv = am > 0.f ? __fdiv_rn(kE4M3Max, am) : 0.f;
+  scale_rows<D>(v, inv);
   uint32_t w[D / 4];
 #pragma unroll
-  for (int j = 0; j < D / 4; ++j)
-    w[j] = e4m3x4(__fmul_rn(v[4 * j], inv), __fmul_rn(v[4 * j + 1], inv), __fmul_rn(v[4 * j + 2], inv),
-                  __fmul_rn(v[4 * j + 3], inv));
+  for (int j = 0; j < D / 4; ++j) w[j] = e4m3x4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
 
   if (x < 2) {
     // codes of row r (D bytes, D / 16 chunks) to swizzled chunk positions,
