@@ -73,12 +73,13 @@ def test_rotation_is_orthogonal_and_keeps_the_scores():
     assert np.abs(F.unrotate_rows(x.astype(np.float64) @ M, s) - x).max() < 1e-12
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("rotate", [False, True])
-def test_quantize_block_properties(rotate):
-    wl = W.Workload("q", B=2, H=3, N=300, seed=11)
+def test_quantize_block_properties(rotate, d):
+    wl = W.Workload("q", B=2, H=3, N=300, d=d, seed=11)
     x = W.make_inputs(wl, grads=False)["q"].float().numpy()
     x[1, 2, 128:256] = 0.0                                              # an all-zero block
-    s = W.rotation_signs(64, 1) if rotate else None
+    s = W.rotation_signs(d, 1) if rotate else None
     codes, scale = F.quantize(x, s)
     assert codes.shape == x.shape and scale.shape == (2, 3, 3) and scale.dtype == np.float32
     assert scale[1, 2, 1] == 0 and not codes[1, 2, 128:256].any()
@@ -99,7 +100,7 @@ def test_quantize_block_properties(rotate):
     c_t, s_t = F.quantize(x, s, per_tensor=True)
     assert np.all(s_t == s_t.flat[0]) and s_t.flat[0] == np.float32(np.abs(xr).max()) / np.float32(448)
     vt = F.transpose_v(codes)
-    assert vt.shape == (2, 3, 64, 384) and not vt[..., 300:].any()
+    assert vt.shape == (2, 3, d, 384) and not vt[..., 300:].any()
     assert np.array_equal(vt[0, 1, :, :300], codes[0, 1].T)
 
 
