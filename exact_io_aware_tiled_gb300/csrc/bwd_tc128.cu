@@ -405,6 +405,16 @@ bwd_tc128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                              have ? __uint_as_float(kraw[2 * c + 1]) * a.scale : 0.f);
         wv[c] = Cvt<T>::pack(have ? __uint_as_float(vraw[2 * c]) : 0.f, have ? __uint_as_float(vraw[2 * c + 1]) : 0.f);
       }
+      if (a.dkv_v8) {
+        // one 32-byte store per tensor: whole sectors in one instruction
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                     :: "l"(static_cast<T*>(a.dk) + off), "r"(wk[0]), "r"(wk[1]), "r"(wk[2]), "r"(wk[3]),
+                        "r"(wk[4]), "r"(wk[5]), "r"(wk[6]), "r"(wk[7]) : "memory");
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                     :: "l"(static_cast<T*>(a.dv) + off), "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3]),
+                        "r"(wv[4]), "r"(wv[5]), "r"(wv[6]), "r"(wv[7]) : "memory");
+        return;
+      }
       uint4* dk = reinterpret_cast<uint4*>(static_cast<T*>(a.dk) + off);
       uint4* dv = reinterpret_cast<uint4*>(static_cast<T*>(a.dv) + off);
       dk[0] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
