@@ -215,3 +215,28 @@ def test_fp8_small_buffers_are_refused(lib):
     assert lib.fa_fwd_fp8(ctypes.byref(p), ctypes.byref(f), ws, 256, FAKE, FAKE, ws, 1 << 30, None) == 4
     assert lib.fa_fwd_fp8(ctypes.byref(p), ctypes.byref(f), ws, 1 << 30, FAKE, FAKE, ws, 16, None) == 4
     assert lib.fa_fwd_fp8(ctypes.byref(p), None, ws, 1 << 30, FAKE, FAKE, ws, 1 << 30, None) == 1
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_views_follow_the_library_layout(lib, d):
+    import torch
+    import exact_io_aware_tiled_gb300 as fa
+    q = torch.empty((2, 4, 300, d), dtype=torch.bfloat16)
+    k = torch.empty((2, 2, 300, d), dtype=torch.bfloat16)
+    p = fa.make_params(q, k=k)
+    lay = fa.fp8_layout(p)
+    buf = torch.zeros(lay["total"], dtype=torch.uint8)
+    v = fa.fp8_views(buf, lay, 2, 4, 2, 300, d)
+    nt, npad = 3, 384
+    shapes = dict(q8=(2, 4, 300, d), k8=(2, 2, 300, d), v8t=(2, 2, d, npad), sq=(2, 4, nt), sk=(2, 2, nt),
+                  sv=(2, 2, nt))
+    base = buf.data_ptr()
+    spans = []
+    for name, shp in shapes.items():
+        t = v[name]
+        assert tuple(t.shape) == shp and t.is_contiguous(), name
+        assert t.data_ptr() - base == lay[name], name
+        spans.append((t.data_ptr() - base, t.data_ptr() - base + t.numel() * t.element_size()))
+    spans.sort()
+    assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))     # no overlap
+    assert spans[-1][1] <= lay["amax"] < lay["total"]
