@@ -30,6 +30,8 @@ MUTATIONS = [
     ("philox.py", "c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0",
      "c0, c1, c2, c3 = hi0 ^ c1 ^ k0, lo1, hi1 ^ c3 ^ k1, lo0"),
     ("philox.py", "return half >= np.uint64(T)", "return half > np.uint64(T)"),
+    ("philox.py", "32: dict(M0=0xD2511F53, M1=0xCD9E8D57", "32: dict(M0=0xD2511F55, M1=0xCD9E8D57"),
+    ("philox.py", "W0=0x9E3779B9, W1=0xBB67AE85", "W0=0x9E3779B9, W1=0xBB67AE86"),
     ("masks.py", "m &= cols > rows - int(window)", "m &= cols >= rows - int(window)"),
     ("attention.py", "dk[b, h // g] += r[\"dk\"]", "dk[b, h // g] = r[\"dk\"]"),
     ("attention.py", "O[b, h], L[b, h] = head_forward(spec, b, h, q[b, h], k[b, h // g], v[b, h // g])",
