@@ -28,15 +28,27 @@ R4  A block is 128 rows x d of one head (the kernel's tile).  Its scale is
     has scale 0 and codes 0.
 R5  The per-tensor baseline has one scale for a whole tensor ([B, H, N, d])
     and no rotation.
-R6  P is quantised too, as FlashAttention-3 does for its second product.
-    The forward is the pages' Q-outer online softmax (ascending key tiles,
-    running row max m, accumulator rescaled by exp(m_old - m_new) whenever m
-    grows).  At key tile t the unnormalised probabilities exp(S - m) lie in
-    (0, 1]; they are multiplied by c_t = 256 sv_t / SV, where sv_t is the V
-    scale of tile t and SV the largest V scale of the head, and rounded to
-    E4M3 (A <= 256 < 448).  Folding sv_t / SV into P lets one accumulator
-    serve key tiles with different V scales.  The row sum l uses the
-    unquantised probabilities, and O' = (SV / 256) * sum_t alpha_t A_t V8_t / l.
+R6  P is quantised too, as FlashAttention-3 does for its second product;
+    the pages do not say on which scale.  The plainest reading rounds the
+    unnormalised probabilities exp(S - m) in (0, 1] (m a running row max
+    no larger than the final one) to E4M3 directly: a relative error of at
+    most 2^-4 (half of the 3-bit mantissa's spacing) in the normal range and
+    at most 2^-10 absolute below 2^-6.  Normalised by the unrounded row sum
+    l_i = sum_j exp(S_ij - m_i) >= 1, the weight of key j then errs by
+        b_ij = max(2^-4 P_ij, 2^-10 / l_i).
+    An implementation that rounds on a grid at least as fine (a larger
+    scale before the rounding) stays inside the same bound.  The gate
+    (``head_forward``) is therefore exact attention of the dequantised,
+    rotated inputs, rotated back, with two bounds on the difference:
+      worst case   |dO_ic| <= sum_j b_ij |V'_jc|;
+      RMS          E[dO_ic^2] <= sum_j b_ij^2 V'_jc^2 / 3
+                   (a rounding error with spacing s has variance s^2 / 12,
+                   and s <= 2 b_ij);
+    where V' is in the output's coordinates: the rows of the dequantised,
+    rotated V multiplied back by M^T (an error in key j's weight moves the
+    whole row, so this is exact under the rotation).  One particular scaling of
+    P (the GPU kernel's) is written out in ``scaled_p_model_forward`` as a
+    diagnostic only; no test gates on it.
 R7  The quantiser decides integer codes from floating-point values, so it
     works in float32 in a fixed order, as the kernel does: the sign flip,
     the fast Walsh-Hadamard butterflies (stage h = 1, 2, ..., d/2 pairs
@@ -49,11 +61,13 @@ Pinned by tests/test_oracle_fp8.py: every E4M3 code decodes as the format
 defines and agrees with torch's float8_e4m3fn; rounding agrees with torch's
 cast on random values and on exact midpoints; the butterflies equal the
 Sylvester matrix product; M is orthogonal and the scores survive the
-rotation; each nonzero block's largest code is 448; with P left unrounded
-the FP8 forward equals the exact attention of the dequantised inputs; equal
-scores return the mean of the dequantised V; and with outliers in the
-inputs, block scales with the rotation give less error than one scale per
-tensor.
+rotation; each nonzero block's largest code is 448; the gate equals exact
+attention (oracle.attention) of the dequantised inputs rotated back; an
+independent simulation that rounds exp(S - m) to E4M3 (final or running
+max) stays inside both bounds of R6, while a coarser rounding or a 1 %
+scale error breaks them; equal scores return the mean of the dequantised
+V; and with outliers in the inputs, block scales with the rotation give
+less error than one scale per tensor.
 """
 from __future__ import annotations
 
@@ -63,7 +77,6 @@ from . import attention as _attn
 
 E4M3_MAX = 448.0
 TILE = 128
-P_SCALE = 256.0
 
 
 # ----------------------------------------------------------------------------
@@ -206,22 +219,86 @@ def dequantize(codes, scale, tile=TILE) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
-# FP8 forward (R3, R6)
+# FP8 forward: the gate (R3, R6)
 # ----------------------------------------------------------------------------
-def head_forward(spec, b, h, q8, sq, k8, sk, v8, sv, signs=None, rows=None,
-                 round_p=True, tie_rel=3e-5):
-    """O, LSE and a per-element rounding allowance for one head of the FP8 forward.
+def head_forward(spec, b, h, q8, sq, k8, sk, v8, sv, signs=None, rows=None):
+    """Exact attention of one head's dequantised FP8 inputs, and the bounds of R6.
 
     q8 [N, d] codes and sq [nt] scales of query head h; k8, v8 [N, d] and
     sk, sv [nt] of its K/V head (row-major V codes).  signs: the rotation
-    the quantiser applied (None for none); O is rotated back with it.
-    round_p=False leaves the probabilities unrounded (a test hook).
+    the quantiser applied (None for none); the output is rotated back with
+    it.  Returns (O, LSE, worst, var) for query ``rows``: O [R, d] and LSE
+    [R] in float64; worst [R, d] the worst-case bound and var [R, d] the
+    variance bound of the error that rounding the probabilities to E4M3
+    adds (R6).
+    """
+    N, d = q8.shape
+    rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
+    cols = np.arange(N)
+    qd, kd = dequantize(q8, sq), dequantize(k8, sk)
+    # V rows rotated back (x M^T): the error of key j's weight moves the
+    # whole row V_j, so the bounds use the rows in the output's coordinates
+    vb = dequantize(v8, sv)
+    if signs is not None:
+        vb = unrotate_rows(vb, signs)
+    O = np.zeros((rows.size, d))
+    worst = np.zeros((rows.size, d))
+    var = np.zeros((rows.size, d))
+    lse = np.zeros(rows.size)
+    for s0 in range(0, rows.size, _attn.ROW_CHUNK):
+        r = rows[s0:s0 + _attn.ROW_CHUNK]
+        vis = _attn.visible(spec, b, r, cols)
+        S = spec.tau * (qd[r] @ kd.T)
+        P, lse[s0:s0 + r.size] = _attn._softmax_rows(S, vis)
+        m = np.where(vis, S, -np.inf).max(axis=1, initial=-np.inf)
+        fin = np.isfinite(m)
+        ls, ms = np.where(fin, lse[s0:s0 + r.size], 0.0), np.where(fin, m, 0.0)
+        ell = np.where(fin, np.exp(ls - ms), 1.0)                  # sum_j exp(S_ij - m_i)
+        bnd = np.where(vis, np.maximum(2.0 ** -4 * P, 2.0 ** -10 / ell[:, None]), 0.0)
+        O[s0:s0 + r.size] = P @ vb
+        worst[s0:s0 + r.size] = bnd @ np.abs(vb)
+        var[s0:s0 + r.size] = (bnd * bnd) @ (vb * vb) / 3.0
+    return O, lse, worst, var
 
-    The allowance bounds what an implementation that computes the
-    probabilities in float32 may differ by: an element whose c_t exp(S - m)
-    lies within a relative ``tie_rel`` of an E4M3 rounding boundary may round
-    either way, and the allowance adds, for every such element, the change
-    in O that the other choice makes.
+
+def attention_fwd(spec, q, k, v, signs=None, per_tensor=False):
+    """Quantise the whole problem and run the gate on every head.
+
+    q [B, H, N, d], k and v [B, H_kv, N, d] (stored-dtype values).  Returns
+    (O, LSE, worst, var, quantised) where quantised holds the codes and
+    scales of q, k and v.
+    """
+    q8, sq = quantize(q, signs, per_tensor)
+    k8, sk = quantize(k, signs, per_tensor)
+    v8, sv = quantize(v, signs, per_tensor)
+    B, H, N, d = q8.shape
+    g = spec.group
+    out = [np.zeros((B, H, N, d)), np.zeros((B, H, N)), np.zeros((B, H, N, d)), np.zeros((B, H, N, d))]
+    for b in range(B):
+        for h in range(H):
+            hk = h // g
+            res = head_forward(spec, b, h, q8[b, h], sq[b, h], k8[b, hk], sk[b, hk], v8[b, hk], sv[b, hk], signs)
+            for o, x in zip(out, res):
+                o[b, h] = x
+    return (*out, dict(q8=q8, sq=sq, k8=k8, sk=sk, v8=v8, sv=sv))
+
+
+# ----------------------------------------------------------------------------
+# one scaling of the rounded probabilities, written out as a diagnostic
+# ----------------------------------------------------------------------------
+P_SCALE = 256.0
+
+
+def scaled_p_model_forward(spec, b, h, q8, sq, k8, sk, v8, sv, signs=None, rows=None, round_p=True):
+    """O and LSE of one head when P is rounded on one particular scale (diagnostic).
+
+    The pages leave the scale of the rounded probabilities open (R6).  This
+    models one choice: the Q-outer online softmax over ascending 128-key
+    tiles rounds exp(S - m) * c_t to E4M3, m the running row max after tile
+    t, c_t = 256 sv_t / SV (sv_t the tile's V scale, SV the head's largest),
+    so that one accumulator serves tiles with different V scales; the row
+    sum uses the unrounded probabilities and O' = (SV / 256) sum_t alpha_t
+    A_t V8_t / l.  It predicts what such a kernel returns; it is not a gate.
     """
     N, d = q8.shape
     tau = spec.tau
@@ -237,7 +314,6 @@ def head_forward(spec, b, h, q8, sq, k8, sk, v8, sv, signs=None, rows=None,
     nt = sv.size
     O = np.zeros((rows.size, d))
     lse = np.zeros(rows.size)
-    allow = np.zeros((rows.size, d))
     for s0 in range(0, rows.size, _attn.ROW_CHUNK):
         r = rows[s0:s0 + _attn.ROW_CHUNK]
         S = tau * (qd[r] @ kd.T)
@@ -259,32 +335,14 @@ def head_forward(spec, b, h, q8, sq, k8, sk, v8, sv, signs=None, rows=None,
         ell_safe = np.where(empty, 1.0, ell)
         W = alpha * A * (SV / P_SCALE) / ell_safe[:, None]
         Orot = np.where(empty[:, None], 0.0, W @ v8d)
-        if round_p:
-            lo = e4m3_round(X * (1.0 - tie_rel))
-            hi = e4m3_round(X * (1.0 + tie_rel))
-            dA = np.where(vis, hi - lo, 0.0)
-            allow_rot = (alpha * dA * (SV / P_SCALE) / ell_safe[:, None]) @ np.abs(v8d)
-        else:
-            allow_rot = np.zeros_like(Orot)
-        if signs is not None:
-            Oc = unrotate_rows(Orot, signs)
-            # |(dO' M^T)_c| <= sum_c' |dO'_c'| / sqrt(d)
-            allow_c = np.repeat(allow_rot.sum(axis=1, keepdims=True) / np.sqrt(d), d, axis=1)
-        else:
-            Oc, allow_c = Orot, allow_rot
+        Oc = unrotate_rows(Orot, signs) if signs is not None else Orot
         O[s0:s0 + r.size] = Oc
-        allow[s0:s0 + r.size] = np.where(empty[:, None], 0.0, allow_c)
         lse[s0:s0 + r.size] = np.where(empty, -np.inf, mfin_safe + np.log(ell_safe))
-    return O, lse, allow
+    return O, lse
 
 
-def attention_fwd(spec, q, k, v, signs=None, per_tensor=False, round_p=True):
-    """Quantise the whole problem and run the FP8 forward on every head.
-
-    q [B, H, N, d], k and v [B, H_kv, N, d] (stored-dtype values).  Returns
-    (O, LSE, allowance, quantised) where quantised holds the codes and
-    scales of q, k and v.
-    """
+def scaled_p_model_attention_fwd(spec, q, k, v, signs=None, per_tensor=False, round_p=True):
+    """``scaled_p_model_forward`` over the whole problem: (O, LSE, quantised)."""
     q8, sq = quantize(q, signs, per_tensor)
     k8, sk = quantize(k, signs, per_tensor)
     v8, sv = quantize(v, signs, per_tensor)
@@ -292,13 +350,12 @@ def attention_fwd(spec, q, k, v, signs=None, per_tensor=False, round_p=True):
     g = spec.group
     O = np.zeros((B, H, N, d))
     L = np.zeros((B, H, N))
-    Al = np.zeros((B, H, N, d))
     for b in range(B):
         for h in range(H):
             hk = h // g
-            O[b, h], L[b, h], Al[b, h] = head_forward(spec, b, h, q8[b, h], sq[b, h], k8[b, hk], sk[b, hk],
+            O[b, h], L[b, h] = scaled_p_model_forward(spec, b, h, q8[b, h], sq[b, h], k8[b, hk], sk[b, hk],
                                                       v8[b, hk], sv[b, hk], signs, round_p=round_p)
-    return O, L, Al, dict(q8=q8, sq=sq, k8=k8, sk=sk, v8=v8, sv=sv)
+    return O, L, dict(q8=q8, sq=sq, k8=k8, sk=sk, v8=v8, sv=sv)
 
 
 def relative_error(approx, exact) -> float:

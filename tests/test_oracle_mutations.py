@@ -44,6 +44,12 @@ MUTATIONS = [
     ("fp8.py", "z[..., 1, :] = a - b", "z[..., 1, :] = b - a"),
     ("fp8.py", "scale = (amax / f448).astype(np.float32)", "scale = (amax / np.float32(240)).astype(np.float32)"),
     ("fp8.py", "Oc = unrotate_rows(Orot, signs)", "Oc = Orot"),
+    ("fp8.py", "np.maximum(2.0 ** -4 * P, 2.0 ** -10 / ell[:, None])",
+     "np.maximum(2.0 ** -5 * P, 2.0 ** -10 / ell[:, None])"),
+    ("fp8.py", "var[s0:s0 + r.size] = (bnd * bnd) @ (vb * vb) / 3.0",
+     "var[s0:s0 + r.size] = (bnd * bnd) @ (vb * vb) / 12.0"),
+    ("fp8.py", "        vb = unrotate_rows(vb, signs)\n", "        pass\n"),
+    ("fp8.py", "O[s0:s0 + r.size] = P @ vb", "O[s0:s0 + r.size] = P @ vb * 1.001"),
     ("fp8.py", "c = P_SCALE * sv / SV if SV > 0 else np.zeros_like(sv)", "c = P_SCALE * np.ones_like(sv)"),
     ("fp8.py", "mrun = np.maximum.accumulate(tmax, axis=1)",
      "mrun = np.repeat(tmax.max(axis=1, keepdims=True), nt, axis=1)"),
