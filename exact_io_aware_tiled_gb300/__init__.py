@@ -8,6 +8,6 @@ ctypes binding plus the seeded synthetic workload generators.
 """
 from ._lib import (FAError, bwd, check_status, dropout_mask, fwd, load, make_params,  # noqa: F401
                    status_string, EXPORTED, DTYPE_CODE)
-from ._lib import bwd_noalloc, selftest_wait_timeout  # noqa: F401
+from ._lib import bwd_noalloc, noalloc_check_status, noalloc_scratch, selftest_wait_timeout  # noqa: F401
 from ._lib import fp8_layout, fp8_quantize, fp8_views, fwd_fp8  # noqa: F401
 from ._build import build, LIB  # noqa: F401

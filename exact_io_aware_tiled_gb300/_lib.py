@@ -21,6 +21,7 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_WORKSPA
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 EXPORTED = ["fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_fwd", "fa_bwd", "fa_bwd_noalloc",
+            "fa_noalloc_check_status", "fa_noalloc_scratch",
             "fa_check_status", "fa_dropout_mask", "fa_selftest_wait_timeout", "fa_status_string", "fa_version",
             "fa_fp8_buffer_layout", "fa_fp8_quantize", "fa_fwd_fp8"]
 
@@ -140,13 +141,22 @@ def make_params(q: torch.Tensor, *, k: Optional[torch.Tensor] = None, causal=Fal
 
 
 def _same_layout(ts):
-    """Tensors of one group must share one stride set with a contiguous last dim."""
+    """Tensors of one group must share one stride set with a contiguous last dim.
+
+    The C ABI takes one stride set per group (q, o, dO, dQ and k, v, dK, dV),
+    so tensors that differ would need a copy.  No copy is made here: that
+    would be hidden HBM traffic on every call.  A mismatch raises instead."""
     ref = ts[0]
-    ok = all(t.shape == ref.shape and t.stride() == ref.stride() and t.dtype == ref.dtype for t in ts)
-    ok = ok and ref.stride(3) == 1
-    if ok:
-        return ts
-    return [t.contiguous() for t in ts]
+    for t in ts:
+        if t.shape != ref.shape or t.dtype != ref.dtype:
+            raise ValueError("tensors of one group must share shape and dtype: %s %s vs %s %s"
+                             % (tuple(t.shape), t.dtype, tuple(ref.shape), ref.dtype))
+        if t.stride() != ref.stride():
+            raise ValueError("tensors of one group must share their strides (%s vs %s); make them "
+                             "alike, e.g. with .contiguous() on each" % (t.stride(), ref.stride()))
+    if ref.stride(3) != 1:
+        raise ValueError("the last dimension must be contiguous (stride 1), got strides %s" % (ref.stride(),))
+    return ts
 
 
 def _layouts(q_like, kv):
@@ -286,19 +296,24 @@ def dropout_mask(B, H, N, b, h, row0, nrows, *, dropout_p, seed=0, offset=0, dev
     return out
 
 
-def selftest_wait_timeout(device="cuda", stream=None):
-    """Run fa_selftest_wait_timeout: returns (status, gave_up[2], waited_ns of the second warp)."""
+def selftest_wait_timeout(device="cuda", stream=None, ws_ptr=None):
+    """Run fa_selftest_wait_timeout: returns (status, gave_up[2], waited_ns of the second warp).
+
+    ws_ptr: a raw device address of at least 256 bytes to use as the
+    workspace (e.g. the fixed array of ``noalloc_scratch``); default a fresh
+    256-byte tensor."""
     lib = load()
     fn = lib.fa_selftest_wait_timeout
     fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     fn.restype = ctypes.c_int
-    ws = torch.empty(256, device=device, dtype=torch.uint8)
+    ws = torch.empty(256, device=device, dtype=torch.uint8) if ws_ptr is None else None
+    wsp = _ptr(ws) if ws_ptr is None else ctypes.c_void_p(int(ws_ptr))
     out = torch.zeros(2, device=device, dtype=torch.int32)
     ns = torch.zeros(1, device=device, dtype=torch.int64)
-    st = fn(_ptr(ws), _ptr(out), _ptr(ns), _stream(stream))
+    st = fn(wsp, _ptr(out), _ptr(ns), _stream(stream))
     if st != FA_OK:
         raise FAError(st, "fa_selftest_wait_timeout")
-    status = check_status(ws, stream)
+    status = lib.fa_check_status(wsp, _stream(stream))
     return status, out.cpu().tolist(), int(ns.item())
 
 
@@ -328,6 +343,29 @@ def bwd_noalloc(q, k, v, o, do, lse, *, causal=False, seqlens_k=None, dropout_p=
     if st != FA_OK:
         raise FAError(st, "fa_bwd_noalloc")
     return dq, dk, dv
+
+
+def noalloc_check_status(stream=None) -> int:
+    """Synchronise and return the status word the last bwd_noalloc on the
+    current device left in the library's fixed scratch array."""
+    lib = load()
+    fn = lib.fa_noalloc_check_status
+    fn.argtypes = [ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn(_stream(stream))
+
+
+def noalloc_scratch():
+    """(device address, bytes) of the fixed scratch array on the current device."""
+    lib = load()
+    fn = lib.fa_noalloc_scratch
+    fn.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_size_t)]
+    fn.restype = ctypes.c_int
+    a, n = ctypes.c_void_p(), ctypes.c_size_t()
+    st = fn(ctypes.byref(a), ctypes.byref(n))
+    if st != FA_OK:
+        raise FAError(st, "fa_noalloc_scratch")
+    return int(a.value), int(n.value)
 
 
 def _fp8_args(q, signs, per_tensor):

@@ -12,49 +12,41 @@
 // How: the array below is a file-scope static __device__ object of
 // kNoAllocScratchBytes bytes.  The CUDA runtime reserves it on every device
 // that loads this library's device code and keeps it there until the process
-// exits.  Host code only knows a host-side stand-in for its name, so before
-// the first use on a device we ask the runtime for its device address
-// (cudaGetSymbolAddress, with that device current) and cache the address per
-// device.  The cached address is then handed to the unchanged fa_bwd path as
-// its workspace.
+// exits.  Host code only knows a host-side stand-in for its name, so every
+// call asks the runtime for its device address on the current device
+// (cudaGetSymbolAddress).  The address is not cached: a device reset or a
+// re-created primary context reloads the module, and the array may then sit
+// elsewhere.  The address is handed to the unchanged fa_bwd path as its
+// workspace.
 //
 // Contract (stated in include/fa.h as well):
 //   * problems whose workspace would exceed kNoAllocScratchBytes are refused
 //     with FA_ERR_WORKSPACE and nothing is enqueued;
-//   * the first call on a device does the address look-up; make that first
-//     call before capturing a stream into a CUDA graph;
+//   * the first call on a device loads the module's device image and looks
+//     up the address; make that first call before capturing a stream into a
+//     CUDA graph;
 //   * every call on a device shares the one array and leaves its contents
 //     behind: fa_bwd clears what must start at zero (status word, dQ
 //     accumulator) on the stream before using it, but two calls whose work
 //     overlaps on the GPU (different streams, no ordering between them) race
 //     on the array and produce garbage.  Serialise them;
+//   * the status word (a bounded device wait that gave up) sits at the start
+//     of the array; fa_noalloc_check_status reads it;
 //   * no cudaMalloc, cudaFree or other allocating call is made.
-#include <mutex>
-
 #include "fa_internal.h"
 
 namespace fa {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;   // 64 MiB per device
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
-
-// Device address of g_noalloc_scratch on the current device (cached).
+// Device address of g_noalloc_scratch on the current device.
 fa_status scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
-    g_addr[dev] = p;
-  }
-  *out = g_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+  *out = p;
   return FA_OK;
 }
 
@@ -72,6 +64,21 @@ fa_status fa_bwd_noalloc(const fa_params* p, const void* q, const void* k, const
   const fa_status s = fa::scratch_address(&ws);
   if (s != FA_OK) return s;
   return fa_bwd(p, q, k, v, o, dout, lse, dq, dk, dv, ws, fa::kNoAllocScratchBytes, stream);
+}
+
+fa_status fa_noalloc_check_status(void* stream) {
+  void* ws = nullptr;
+  const fa_status s = fa::scratch_address(&ws);
+  if (s != FA_OK) return s;
+  return fa_check_status(ws, stream);
+}
+
+fa_status fa_noalloc_scratch(void** addr, size_t* bytes) {
+  if (addr == nullptr || bytes == nullptr) return FA_ERR_INVALID_ARG;
+  const fa_status s = fa::scratch_address(addr);
+  if (s != FA_OK) return s;
+  *bytes = fa::kNoAllocScratchBytes;
+  return FA_OK;
 }
 
 }  // extern "C"

@@ -172,19 +172,37 @@ fa_status fa_bwd(const fa_params *p, const void *q, const void *k, const void *v
  * device that loads the library holds that array until the process exits.
  * Arguments are those of fa_bwd without ws / ws_bytes.
  *   - Returns FA_ERR_WORKSPACE, enqueuing nothing, when
- *     fa_bwd_workspace_size(p) exceeds 64 MiB (roughly B*H*N > 240,000 rows
- *     for 16-bit inputs).
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     fa_bwd_workspace_size(p) exceeds 64 MiB.  For 16-bit inputs the
+ *     scratch is about 264 bytes per query row at d = 64 and 520 at
+ *     d = 128 (float32 dQ accumulator, LSE and D), so B*H*N may reach about
+ *     254,000 rows at d = 64 and 129,000 at d = 128; float32 inputs need
+ *     8 bytes per row.  Block-sparse masks add their block lists.
+ *   - The array's device address is looked up on every call (with the
+ *     calling thread's current device).  The first call on a device also
+ *     loads the library's device image there; make that first call before
+ *     any stream capture.
  *   - All calls on a device share the array and leave their contents in it;
  *     what must start at zero is cleared on the stream by each call, but
  *     calls whose GPU work overlaps (unordered streams) race on it.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
- * fa_check_status cannot be used with it (there is no caller workspace).
+ *   - A bounded device wait that gives up records FA_ERR_TIMEOUT in the
+ *     array's status word: read it with fa_noalloc_check_status.
  * ------------------------------------------------------------------------- */
 fa_status fa_bwd_noalloc(const fa_params *p, const void *q, const void *k, const void *v,
                          const void *o, const void *dout, const float *lse,
                          void *dq, void *dk, void *dv, void *stream);
+
+/* fa_noalloc_check_status -- fa_check_status for fa_bwd_noalloc: synchronises
+ * `stream`, then returns the status word the last fa_bwd_noalloc on the
+ * current device left in the fixed array (FA_OK, or FA_ERR_TIMEOUT if a
+ * bounded device wait ran out; the gradients are then undefined).
+ * FA_ERR_CUDA if the stream reported an error. */
+fa_status fa_noalloc_check_status(void *stream);
+
+/* fa_noalloc_scratch -- the current device's address and size of the fixed
+ * array fa_bwd_noalloc uses (for diagnostics: e.g. to run
+ * fa_selftest_wait_timeout on it).  Allocates nothing. */
+fa_status fa_noalloc_scratch(void **addr, size_t *bytes);
 
 /* ---------------------------------------------------------------------------
  * fa_check_status -- synchronises `stream`, then reads the status word the

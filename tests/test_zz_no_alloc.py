@@ -3,11 +3,15 @@
 Some callers cannot hand fa_bwd a workspace (they run inside a memory pool
 they do not own, in a hook where allocation is forbidden, or from plain C
 without a device allocator).  fa_bwd_noalloc takes its scratch from a fixed
-array inside the library instead.  This test calls it through the C ABI
-twice in a row and checks both results against the ordinary fa_bwd, with the
-gradient tolerance of the other parity tests; it also checks that a problem
-too large for the fixed array is refused before anything runs.  The file is
-named so that pytest collects it last.
+array inside the library instead.  These tests call it through the C ABI
+twice in a row and check both results against the ordinary fa_bwd, with the
+gradient tolerance of the other parity tests; run a sequence of different
+problems (block-sparse, head dimension 128, a smaller causal one) through
+the one shared array, each against fa_bwd with its own workspace; check that
+a timeout recorded in the array's status word is reported by
+fa_noalloc_check_status and cleared by the next call; and check that a
+problem too large for the fixed array is refused before anything runs.  The
+file is named so that pytest collects it last.
 """
 import ctypes
 
@@ -58,6 +62,41 @@ def test_noalloc_backward_float32_path():
         got = fa.bwd_noalloc(inp["q"], inp["k"], inp["v"], o, inp["do"], lse)
         torch.cuda.synchronize()
         _grads_match(got, ref, TOL["f32"]["grad"])
+
+
+def test_noalloc_reuses_the_array_across_different_problems():
+    """The shared array keeps what the previous call left: block lists, the
+    work counter, the dQ accumulator.  Each problem must still match fa_bwd
+    with a fresh workspace of its own."""
+    seq = [W.Workload("nz_sparse", B=1, H=2, N=640, dtype="bf16", sparse_butterfly=True, seed=21),
+           W.Workload("nz_d128", B=1, H=2, N=300, d=128, dtype="bf16", seed=22),
+           W.Workload("nz_causal", B=1, H=1, N=200, dtype="f16", causal=True, seed=23),
+           W.Workload("nz_sparse_again", B=2, H=1, N=384, dtype="bf16", sparse_butterfly=True, causal=True,
+                      seed=24)]
+    for wl in seq:
+        inp = {k: v.cuda() for k, v in W.make_inputs(wl).items()}
+        kw = kwargs_of(wl)
+        o, lse = fa.fwd(inp["q"], inp["k"], inp["v"], **kw)
+        ref = fa.bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, **kw)
+        got = fa.bwd_noalloc(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, **kw)
+        assert fa.noalloc_check_status() == 0, wl.name
+        _grads_match(got, ref, TOL[wl.dtype]["grad"])
+
+
+def test_noalloc_status_word_reports_a_timeout():
+    addr, nbytes = fa.noalloc_scratch()
+    assert nbytes == 64 << 20 and addr % 256 == 0
+    # the bounded-wait self-test gives up and records FA_ERR_TIMEOUT at the
+    # start of the fixed array, where fa_bwd_noalloc keeps its status word
+    status, gave_up, _ = fa.selftest_wait_timeout(ws_ptr=addr)
+    assert status == _lib.FA_ERR_TIMEOUT and gave_up == [1, 1]
+    assert fa.noalloc_check_status() == _lib.FA_ERR_TIMEOUT
+    # the next backward clears the word before it runs
+    wl = W.Workload("nz_after", B=1, H=1, N=256, dtype="bf16", causal=True, seed=25)
+    inp = {k: v.cuda() for k, v in W.make_inputs(wl).items()}
+    o, lse = fa.fwd(inp["q"], inp["k"], inp["v"], causal=True)
+    fa.bwd_noalloc(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, causal=True)
+    assert fa.noalloc_check_status() == 0
 
 
 def test_noalloc_refuses_problems_larger_than_its_array():
