@@ -27,8 +27,8 @@ and the check bounds the absolute error by 1e-2 (1e-5) of that.  Any other
 set of rows or columns -- every ordinary head -- gets no floor.  dV never
 needs one: dV = P~^T dO has no cancelling sum, and a column no row sees has
 dV = 0, where the error itself (exactly zero on the GPU) is checked.
-The report carries the plain ratio under ``<name>`` and the denominator used
-under ``<name>_den`` ("ref" or "floor").
+The report carries the plain ratio under ``<name>`` and, under
+``<name>_floored``, 1.0 where the floor was the denominator (else 0.0).
 For a K/V head shared by g query heads (grouped-query attention) dK and dV
 sum over the group, and so do their floors, in quadrature.
 """
@@ -150,12 +150,8 @@ def grad_check(report, name, got, ref, floor, tol, vanishes):
     err = float(np.linalg.norm(got - ref))
     nref = float(np.linalg.norm(ref))
     report[name] = err / nref if nref > 0 else err
-    if vanishes:
-        report[name + "_den"] = "floor"
-        ok = err <= tol * max(floor, nref)
-    else:
-        report[name + "_den"] = "ref"
-        ok = err <= tol * nref
+    report[name + "_floored"] = 1.0 if vanishes else 0.0
+    ok = err <= tol * (max(floor, nref) if vanishes else nref)
     assert ok, (name, report)
 
 
