@@ -235,6 +235,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--batch", type=int, default=0, help="override B (small profiling cases)")
+    ap.add_argument("--soak", type=float, default=2.0, help="seconds of back-to-back steps for the per-step "
+                    "distribution and the clocks under load (0: skip)")
+    ap.add_argument("--cold-iters", type=int, default=50, help="steps timed one by one after a 512 MB write "
+                    "(cold L2; 0: skip)")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-config table")
+    ap.add_argument("--config-steps", type=int, default=20, help="timed steps per config of the table")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -259,66 +265,36 @@ def main():
     fa.load()
 
     host = W.make_inputs(wl)
-    t = {k: v.to(dev) for k, v in host.items()}
-    kw = dict(causal=wl.causal, dropout_p=wl.dropout_p, seed=wl.dropout_seed, offset=wl.dropout_offset,
-              window=wl.window,
-              seqlens_k=None if wl.seqlens is None else torch.from_numpy(np.asarray(wl.seqlens, np.int32)).to(dev),
-              block_mask=None if wl.block_mask is None else torch.from_numpy(wl.block_mask.astype(np.uint8)).to(dev))
-    pairs = visible_pairs(wl)
-    fp8 = is_fp8(wl)
-    fwd_flops = 4.0 * wl.d * pairs
-    bwd_flops = 0.0 if fp8 else 10.0 * wl.d * pairs
-    # FP8 workloads are forward only (quantise + forward): their step counts the forward FLOPs
-    step_flops_headline = fwd_flops if fp8 else 2.5 * fwd_flops
-    step_flops_exec = fwd_flops + bwd_flops
+    R = Runner(wl, host, dev)
+    t, kw, step = R.t, R.kw, R.step
+    fp8 = R.fp8
+    fwd_flops, bwd_flops = R.fwd_flops, R.bwd_flops
+    step_flops_headline, step_flops_exec = R.step_flops_headline, R.step_flops_exec
     stream = torch.cuda.current_stream(dev)
     if fp8:
-        kw8 = {k_: v_ for k_, v_ in kw.items() if k_ not in ("dropout_p", "seed", "offset")}
-        signs = torch.from_numpy(W.rotation_signs(wl.d, wl.seed)).to(dev)
-        fp8_buf = torch.empty(fa.fp8_layout(fa.make_params(t["q"], k=t["k"]))["total"], device=dev,
-                              dtype=torch.uint8)
+        kw8, signs, fp8_buf = R.kw8, R.signs, R.fp8_buf
 
-    def step(prof_f=None, prof_b=None, src=None):
-        src = t if src is None else src
-        if fp8:
-            o, lse = fa.fwd_fp8(src["q"], src["k"], src["v"], signs=signs, prof=prof_f, buf=fp8_buf, **kw8)
-            return o, lse, None
-        o, lse = fa.fwd(src["q"], src["k"], src["v"], prof=prof_f, **kw)
-        dq, dk, dv = fa.bwd(src["q"], src["k"], src["v"], o, src["do"], lse, prof=prof_b, **kw)
-        return o, lse, dq
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    st_f = fa.check_status(fa.fwd_fp8.last_workspace if fp8 else fa.fwd.last_workspace)
-    st_b = 0 if fp8 else fa.check_status(fa.bwd.last_workspace)
-    if st_f or st_b:
-        raise SystemExit("device status after warm-up: fwd %d bwd %d" % (st_f, st_b))
+    R.warmup(args.warmup)
 
     K = args.steps
-    evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    for a, b in evf + evb:      # materialise the events so their handles can be passed down
-        a.record(stream)
-        b.record(stream)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clk = ClockSampler(dev.index)
     clk.start()
     time.sleep(0.3)
     _barrier(ws)
     torch.cuda.synchronize()
-    e0.record(stream)
-    for s in range(K):
-        step((evf[s][0].cuda_event, evf[s][1].cuda_event), (evb[s][0].cuda_event, evb[s][1].cuda_event))
-    e1.record(stream)
+    ms, fwd_ms, bwd_ms, _ = R.timed(K)
     torch.cuda.synchronize()
     _barrier(ws)
-    clocks = clk.stop()
-    ms = e0.elapsed_time(e1) / K
-    fwd_ms = sum(a.elapsed_time(b) for a, b in evf) / K
-    bwd_ms = 0.0 if fp8 else sum(a.elapsed_time(b) for a, b in evb) / K
+    timed_region_s = ms * K * 1e-3
     ms_max = _max_over_ranks(ms, ws, dev)
+    # soak: the same step back to back for >= soak_s seconds (per-step events),
+    # so that the clock sampler sees the GPU under load and the per-step
+    # distribution (median, p10, p90) rests on many iterations
+    soak = None
+    if args.soak > 0:
+        soak = R.soak(args.soak)
+    clocks = clk.stop()
+    cold = R.cold_l2(args.cold_iters) if args.cold_iters > 0 else None
 
     # end to end: pinned host inputs -> device, fwd + bwd, O, LSE and the
     # gradients back to pinned host memory, every step.  Consecutive steps
@@ -416,17 +392,45 @@ def main():
                             "device outputs and workspaces allocated once"}
 
     peaks, peak_kind = _peaks()
+    # The K-step timed region lasts well under a second: its kernels run at
+    # the burst clock, so their fractions are taken of the burst peak.  The
+    # soak (seconds back to back, under the power cap) is compared with the
+    # sustained peak.
+    burst_region = timed_region_s < 1.0
+    peak_name = "bf16_tflops" if burst_region else "bf16_tflops_sustained"
+    peak = float(peaks[peak_name])
+    peak_src = "%s %s (timed region %.3f s)" % (peak_kind, peak_name, timed_region_s)
+    if fp8:     # E4M3 products: the bf16 peak x the nominal dense FP8 / BF16 ratio (4.5 / 2.25)
+        peak *= 2.0
+        peak_src += " x 2 (nominal fp8 / bf16 dense ratio)"
     dominant = "bwd" if bwd_ms >= fwd_ms else "fwd"
     kern_ms = bwd_ms if dominant == "bwd" else fwd_ms
     kern_flops = bwd_flops if dominant == "bwd" else fwd_flops
     achieved = kern_flops / (kern_ms * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops_sustained"])
-    peak_src = "%s bf16_tflops_sustained" % peak_kind
-    if fp8:     # E4M3 products: the bf16 peak x the nominal dense FP8 / BF16 ratio (4.5 / 2.25)
-        peak *= 2.0
-        peak_src = "%s bf16_tflops_sustained x 2 (nominal fp8 / bf16 dense ratio)" % peak_kind
     kern_name = ("attn_%s_tc" % dominant) if not fp8 else "attn_fwd_fp8"
     traffic = _recorded_traffic(wl.name, "fwd_fp8" if fp8 else dominant)
+    if soak is not None:
+        sus = float(peaks["bf16_tflops_sustained"]) * (2.0 if fp8 else 1.0)
+        soak["fwd_frac_of_sustained"] = fwd_flops / (soak["fwd_ms"]["median"] * 1e-3) / 1e12 / sus
+        if not fp8:
+            soak["bwd_frac_of_sustained"] = bwd_flops / (soak["bwd_ms"]["median"] * 1e-3) / 1e12 / sus
+        soak["value_median"] = replica_value(ws, step_flops_headline, soak["step_ms"]["median"])
+
+    per_config = None
+    if ws == 1 and not args.no_per_config:
+        per_config = {}
+        for name in PER_CONFIG:
+            if name == wl.name:
+                rr = R
+            else:
+                rr = Runner(W.CONFIGS[name], W.make_inputs(W.CONFIGS[name]), dev)
+                rr.warmup(3)
+            m, f, b_, _ = rr.timed(args.config_steps)
+            per_config[name] = rr.summary(m, f, b_, peaks, args.config_steps)
+            if rr is not R:
+                rr.release()
+            del rr
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
@@ -444,9 +448,9 @@ def main():
         "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "H_kv": wl.hkv, "N": wl.N, "d": wl.d,
                    "causal": wl.causal, "window": wl.window,
                    "dropout_p": wl.dropout_p, "parallelism": "replicas" if ws > 1 else "single",
-                   "l2": "inputs exceed L2 (%.0f MB per step)" % (sum(v.numel() * v.element_size()
-                                                                      for v in host.values()) / 1e6)},
-        "pct_of_bf16_peak": 100.0 * value / float(peaks["bf16_tflops_sustained"]) / ws,
+                   "l2": "inputs exceed L2 (%.0f MB per step); cold-L2 run separately" %
+                         (sum(v.numel() * v.element_size() for v in host.values()) / 1e6)},
+        "pct_of_bf16_peak": 100.0 * value / float(peaks[peak_name]) / ws,
         "value_executed_flops": replica_value(ws, step_flops_exec, ms_max),
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "roofline": {"kernel": kern_name, "bound": "tensor", "achieved": achieved, "peak": peak,
@@ -455,11 +459,196 @@ def main():
         "roofline_fwd": {"achieved": fwd_flops / (fwd_ms * 1e-3) / 1e12, "peak": peak,
                          "frac": fwd_flops / (fwd_ms * 1e-3) / 1e12 / peak},
         "clocks": clocks,
+        "soak": soak,
+        "cold_l2": cold,
+        "per_config": per_config,
         "gpu_launches": _launches_per_step(wl) * K,
         "cpu_baseline": cpu,
         "e2e": e2e,
     }
-    print(json.dumps(line), flush=True)
+    print(json.dumps(line, default=_json_default), flush=True)
+
+
+def _json_default(o):
+    """numpy scalars (e.g. the pair counts) as plain numbers."""
+    if hasattr(o, "item"):
+        return o.item()
+    raise TypeError("not JSON serialisable: %r" % (o,))
+
+
+# The five workloads the per-config table covers (one line each in the JSON
+# object ``per_config``).
+PER_CONFIG = ("tiny_f32", "gpt2_medium_causal", "bert_large_pad_dropout", "long_ragged_causal_f16",
+              "butterfly_sparse_64k")
+
+
+def _pct(xs, q):
+    xs = sorted(xs)
+    if not xs:
+        return None
+    k = (len(xs) - 1) * q
+    lo = int(k)
+    hi = min(lo + 1, len(xs) - 1)
+    return xs[lo] + (xs[hi] - xs[lo]) * (k - lo)
+
+
+def _dist_stats(xs):
+    return {"median": _pct(xs, 0.5), "p10": _pct(xs, 0.1), "p90": _pct(xs, 0.9), "n": len(xs)}
+
+
+class Runner:
+    """One workload resident on the device and its fwd(+bwd) step."""
+
+    def __init__(self, wl, host, dev):
+        import torch
+        import exact_io_aware_tiled_gb300 as fa
+        from exact_io_aware_tiled_gb300 import workloads as W
+        self.torch, self.fa, self.wl, self.dev = torch, fa, wl, dev
+        self.t = {k: v.to(dev) for k, v in host.items()}
+        self.kw = dict(causal=wl.causal, dropout_p=wl.dropout_p, seed=wl.dropout_seed, offset=wl.dropout_offset,
+                       window=wl.window,
+                       seqlens_k=None if wl.seqlens is None else
+                       torch.from_numpy(np.asarray(wl.seqlens, np.int32)).to(dev),
+                       block_mask=None if wl.block_mask is None else
+                       torch.from_numpy(wl.block_mask.astype(np.uint8)).to(dev))
+        self.pairs = visible_pairs(wl)
+        self.fp8 = is_fp8(wl)
+        self.fwd_flops = 4.0 * wl.d * self.pairs
+        self.bwd_flops = 0.0 if self.fp8 else 10.0 * wl.d * self.pairs
+        # FP8 workloads are forward only (quantise + forward): their step counts the forward FLOPs
+        self.step_flops_headline = self.fwd_flops if self.fp8 else 2.5 * self.fwd_flops
+        self.step_flops_exec = self.fwd_flops + self.bwd_flops
+        self.stream = torch.cuda.current_stream(dev)
+        if self.fp8:
+            self.kw8 = {k_: v_ for k_, v_ in self.kw.items() if k_ not in ("dropout_p", "seed", "offset")}
+            self.signs = torch.from_numpy(W.rotation_signs(wl.d, wl.seed)).to(dev)
+            self.fp8_buf = torch.empty(fa.fp8_layout(fa.make_params(self.t["q"], k=self.t["k"]))["total"],
+                                       device=dev, dtype=torch.uint8)
+
+    def step(self, prof_f=None, prof_b=None, src=None):
+        fa, src = self.fa, (self.t if src is None else src)
+        if self.fp8:
+            o, lse = fa.fwd_fp8(src["q"], src["k"], src["v"], signs=self.signs, prof=prof_f, buf=self.fp8_buf,
+                                **self.kw8)
+            return o, lse, None
+        o, lse = fa.fwd(src["q"], src["k"], src["v"], prof=prof_f, **self.kw)
+        dq, dk, dv = fa.bwd(src["q"], src["k"], src["v"], o, src["do"], lse, prof=prof_b, **self.kw)
+        return o, lse, dq
+
+    def warmup(self, n):
+        fa, torch = self.fa, self.torch
+        for _ in range(n):
+            self.step()
+        torch.cuda.synchronize()
+        st_f = fa.check_status(fa.fwd_fp8.last_workspace if self.fp8 else fa.fwd.last_workspace)
+        st_b = 0 if self.fp8 else fa.check_status(fa.bwd.last_workspace)
+        if st_f or st_b:
+            raise SystemExit("device status after warm-up (%s): fwd %d bwd %d" % (self.wl.name, st_f, st_b))
+
+    def _events(self, n):
+        torch = self.torch
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+        for e in ev:            # materialise the events so their handles can be passed down
+            for x in e:
+                x.record(self.stream)
+        torch.cuda.synchronize()
+        return ev
+
+    def timed(self, K, ev=None, between=None):
+        """K steps back to back (or with ``between()`` before each, untimed):
+        mean step ms over the whole region, mean fwd / bwd kernel ms, and the
+        per-step kernel times.  Events inside the calls bracket the main
+        kernels on the launching stream."""
+        torch = self.torch
+        ev = self._events(K) if ev is None else ev
+        steps = []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if between is None:
+            e0.record(self.stream)
+            for s in range(K):
+                self.step((ev[s][0].cuda_event, ev[s][1].cuda_event), (ev[s][2].cuda_event, ev[s][3].cuda_event))
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / K
+        else:
+            marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+            for s in range(K):
+                between()
+                marks[s][0].record(self.stream)
+                self.step((ev[s][0].cuda_event, ev[s][1].cuda_event), (ev[s][2].cuda_event, ev[s][3].cuda_event))
+                marks[s][1].record(self.stream)
+            torch.cuda.synchronize()
+            steps = [a.elapsed_time(b) for a, b in marks]
+            ms = sum(steps) / K
+        fw = [e[0].elapsed_time(e[1]) for e in ev[:K]]
+        bw = [0.0 if self.fp8 else e[2].elapsed_time(e[3]) for e in ev[:K]]
+        return ms, sum(fw) / K, sum(bw) / K, dict(step=steps, fwd=fw, bwd=bw)
+
+    def soak(self, seconds, chunk=50, max_steps=5000):
+        """Steps back to back for about ``seconds``; per-step distributions."""
+        torch = self.torch
+        ev = self._events(chunk)
+        step_ms, fw, bw = [], [], []
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < seconds and n < max_steps:
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(chunk + 1)]
+            marks[0].record(self.stream)
+            for s in range(chunk):
+                self.step((ev[s][0].cuda_event, ev[s][1].cuda_event), (ev[s][2].cuda_event, ev[s][3].cuda_event))
+                marks[s + 1].record(self.stream)
+            torch.cuda.synchronize()
+            step_ms += [marks[s].elapsed_time(marks[s + 1]) for s in range(chunk)]
+            fw += [e[0].elapsed_time(e[1]) for e in ev]
+            bw += [0.0 if self.fp8 else e[2].elapsed_time(e[3]) for e in ev]
+            n += chunk
+        out = {"seconds": round(time.perf_counter() - t0, 3), "step_ms": _dist_stats(step_ms),
+               "fwd_ms": _dist_stats(fw)}
+        if not self.fp8:
+            out["bwd_ms"] = _dist_stats(bw)
+        return out
+
+    def cold_l2(self, iters, scratch_mb=512):
+        """Each step preceded (untimed) by a write of a buffer four times the
+        L2, so the step starts with none of its inputs in L2."""
+        torch = self.torch
+        buf = torch.empty(scratch_mb << 20, dtype=torch.uint8, device=self.dev)
+        flip = [0]
+
+        def between():
+            flip[0] ^= 1
+            buf.fill_(flip[0])
+
+        ms, f, b_, per = self.timed(iters, between=between)
+        del buf
+        out = {"scratch_mb_between_steps": scratch_mb, "step_ms": _dist_stats(per["step"]),
+               "fwd_ms": _dist_stats(per["fwd"])}
+        if not self.fp8:
+            out["bwd_ms"] = _dist_stats(per["bwd"])
+        out["value_median"] = self.step_flops_headline / (out["step_ms"]["median"] * 1e-3) / 1e12
+        return out
+
+    def summary(self, ms, fwd_ms, bwd_ms, peaks, K):
+        burst = float(peaks["bf16_tflops"])
+        wl = self.wl
+        out = {"shape": "B%d H%d%s N%d d%d %s%s%s%s%s" % (
+            wl.B, wl.H, "" if wl.hkv == wl.H else " H_kv%d" % wl.hkv, wl.N, wl.d, wl.dtype,
+            " causal" if wl.causal else "", " window%d" % wl.window if wl.window else "",
+            " padding" if wl.seqlens is not None else "", " butterfly" if wl.block_mask is not None else "")
+            + (" dropout%.2g" % wl.dropout_p if wl.dropout_p else ""),
+            "steps": K, "ms": ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "tflops_literal": self.step_flops_headline / (ms * 1e-3) / 1e12,
+            "tflops_executed": self.step_flops_exec / (ms * 1e-3) / 1e12,
+            "visible_pairs": int(self.pairs)}
+        if wl.dtype == "f32":
+            out["note"] = "float32 path on CUDA cores (FFMA); no tensor-core fraction"
+        else:
+            out["fwd_frac_of_burst"] = self.fwd_flops / (fwd_ms * 1e-3) / 1e12 / burst
+            out["bwd_frac_of_burst"] = self.bwd_flops / (bwd_ms * 1e-3) / 1e12 / burst
+        return out
+
+    def release(self):
+        self.t = None
 
 
 def _launches_per_step(wl):

@@ -236,7 +236,7 @@ def fwd(q, k, v, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=
     seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
     B, H, N, d = q.shape
     if out is not None and not q.is_contiguous():
-        q = q.contiguous()
+        raise ValueError("out= takes contiguous outputs, so q must be contiguous too (o shares q's strides)")
     o, lse = _outputs(out, [q, ((B, H, N), torch.float32, q.device)])
     o32 = torch.empty((B, H, N, d), device=q.device, dtype=torch.float32) if return_o_f32 else None
     p = make_params(q, k=k, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
@@ -259,10 +259,11 @@ def bwd(q, k, v, o, do, lse, *, causal=False, seqlens_k=None, dropout_p=0.0, see
     _check(q)
     (q, o, do), (k, v) = _layouts([q, o, do], [k, v])
     if out is not None and (not q.is_contiguous() or not k.is_contiguous()):
-        q, o, do, k, v = (t.contiguous() for t in (q, o, do, k, v))
+        raise ValueError("out= takes contiguous outputs, so q, o, dO, k and v must be contiguous too")
+    if not lse.is_contiguous():
+        raise ValueError("lse must be the contiguous [B, H, N] float32 tensor fwd returns")
     lib = load()
     seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
-    lse = lse.contiguous()
     dq, dk, dv = _outputs(out, [q, k, v])
     p = make_params(q, k=k, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
                     block_mask=block_mask, scale=scale, prof=prof, window=window)
@@ -334,7 +335,8 @@ def bwd_noalloc(q, k, v, o, do, lse, *, causal=False, seqlens_k=None, dropout_p=
     fn.argtypes = [ctypes.POINTER(fa_params)] + [ctypes.c_void_p] * 10
     fn.restype = ctypes.c_int
     seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
-    lse = lse.contiguous()
+    if not lse.is_contiguous():
+        raise ValueError("lse must be the contiguous [B, H, N] float32 tensor fwd returns")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     p = make_params(q, k=k, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
                     block_mask=block_mask, scale=scale, window=window)
@@ -435,7 +437,7 @@ def fwd_fp8(q, k, v, *, signs=None, per_tensor=False, causal=False, seqlens_k=No
     _check(q)
     (q,), (k, v) = _layouts([q], [k, v])
     if out is not None and not q.is_contiguous():
-        q = q.contiguous()
+        raise ValueError("out= takes contiguous outputs, so q must be contiguous too (o shares q's strides)")
     lib = load()
     seqlens_k, block_mask = _aux(seqlens_k, block_mask, q)
     B, H, N, d = q.shape
