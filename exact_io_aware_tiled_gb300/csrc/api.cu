@@ -130,6 +130,14 @@ DropoutArgs dropout_of(const fa_params* p) {
   DropoutArgs d{};
   d.k0 = (uint32_t)(p->seed & 0xFFFFFFFFu);
   d.k1 = (uint32_t)(p->seed >> 32);
+  // Philox4x32 key schedule (Salmon et al., SC'11): the key is bumped by the
+  // Weyl constants before every round after the first.  It depends on the
+  // seed only, so it is computed once here and the kernels read each round's
+  // key as a constant.
+  for (int r = 0; r < 10; ++r) {
+    d.rk0[r] = d.k0 + (uint32_t)r * 0x9E3779B9u;
+    d.rk1[r] = d.k1 + (uint32_t)r * 0xBB67AE85u;
+  }
   d.off_lo = (uint32_t)(p->offset & 0xFFFFFFFFu);
   d.off_hi = (uint32_t)(p->offset >> 32);
   const double t = std::floor((double)p->dropout_p * 65536.0 + 0.5);

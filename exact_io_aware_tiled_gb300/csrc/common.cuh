@@ -302,15 +302,14 @@ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t col16) {
 struct u32x4 { uint32_t x, y, z, w; };
 
 __device__ __forceinline__ u32x4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                               uint32_t k0, uint32_t k1) {
+                                               const DropoutArgs& dp) {
   constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
-  constexpr uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    if (r > 0) { k0 += W0; k1 += W1; }
+    // round keys k + r W (W the Weyl constants), precomputed on the host
     const uint32_t hi0 = __umulhi(M0, c0), lo0 = M0 * c0;
     const uint32_t hi1 = __umulhi(M1, c2), lo1 = M1 * c2;
-    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    const uint32_t n0 = hi1 ^ c1 ^ dp.rk0[r], n2 = hi0 ^ c3 ^ dp.rk1[r];
     c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
   }
   return {c0, c1, c2, c3};
@@ -318,7 +317,7 @@ __device__ __forceinline__ u32x4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
 
 // 8 keep bits (bit t <-> key 8g + t) for global query row `row_g`, key group g.
 __device__ __forceinline__ uint32_t dropout_keep8(uint32_t g, uint32_t row_g, const DropoutArgs& dp) {
-  const u32x4 r = philox4x32_10(g, row_g, dp.off_lo, dp.off_hi, dp.k0, dp.k1);
+  const u32x4 r = philox4x32_10(g, row_g, dp.off_lo, dp.off_hi, dp);
   const uint32_t w[4] = {r.x, r.y, r.z, r.w};
   uint32_t bits = 0;
 #pragma unroll

@@ -18,6 +18,7 @@ struct Strides { int64_t b, h, n; };
 
 struct DropoutArgs {
   uint32_t k0, k1;         // Philox key = (lo32(seed), hi32(seed))
+  uint32_t rk0[10], rk1[10];  // the key of each of the ten rounds: k + r * (Weyl constant), mod 2^32
   uint32_t off_lo, off_hi; // counter words 2, 3
   uint32_t threshold;      // keep iff 16-bit slice >= threshold
   float rp;                // 1 / (1 - p)
