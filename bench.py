@@ -101,7 +101,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         time.sleep(0.1)
-        sm, smax, reasons = [], None, set()
+        sm, smax, reasons, pw = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -112,11 +112,17 @@ class ClockSampler:
                 smax = float(f[2])
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         loaded = [x for x in sm if smax is None or x > 0.5 * smax] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "sm_mhz_min": min(loaded) if loaded else None,
+                "power_w_median": statistics.median(pw) if pw else None, "power_w_max": max(pw) if pw else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 

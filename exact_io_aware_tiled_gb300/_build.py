@@ -16,8 +16,8 @@ PKG = Path(__file__).resolve().parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libfa_gb300.so"
-SOURCES = ["api.cu", "fwd_tc.cu", "bwd_tc.cu", "bwd_tc128.cu", "simt_f32.cu", "aux_kernels.cu", "noalloc.cu",
-           "fwd_fp8.cu", "fp8_quant.cu"]
+SOURCES = ["api.cu", "fwd_tc.cu", "fwd_tc1.cu", "bwd_tc.cu", "bwd_tc128.cu", "simt_f32.cu", "aux_kernels.cu",
+           "noalloc.cu", "fwd_fp8.cu", "fp8_quant.cu"]
 HEADERS = ["common.cuh", "bwd_items.cuh", "fa_internal.h", "fwd_plan.cuh", "fp8.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -43,6 +43,7 @@ class fa_params(ctypes.Structure):
         ("H_kv", ctypes.c_int32),
         ("kv_stride_b", ctypes.c_int64), ("kv_stride_h", ctypes.c_int64), ("kv_stride_n", ctypes.c_int64),
         ("window", ctypes.c_int32),
+        ("fwd_kernel", ctypes.c_int32),
     ]
 
 
@@ -116,7 +117,8 @@ def _stream(stream):
 
 
 def make_params(q: torch.Tensor, *, k: Optional[torch.Tensor] = None, causal=False, seqlens_k=None, dropout_p=0.0,
-                seed=0, offset=0, block_mask=None, scale=None, o_f32=None, prof=None, window=0) -> fa_params:
+                seed=0, offset=0, block_mask=None, scale=None, o_f32=None, prof=None, window=0,
+                fwd_kernel=0) -> fa_params:
     B, H, N, d = q.shape
     p = fa_params()
     p.B, p.H, p.N, p.d = B, H, N, d
@@ -126,6 +128,7 @@ def make_params(q: torch.Tensor, *, k: Optional[torch.Tensor] = None, causal=Fal
         p.H_kv = k.shape[1]
         p.kv_stride_b, p.kv_stride_h, p.kv_stride_n = k.stride(0), k.stride(1), k.stride(2)
     p.window = int(window)
+    p.fwd_kernel = int(fwd_kernel)
     p.scale = 0.0 if scale is None else float(scale)
     p.causal = 1 if causal else 0
     p.seqlens_k = None if seqlens_k is None else seqlens_k.data_ptr()
@@ -223,13 +226,15 @@ def _workspace(lib_size, workspace, device):
 
 
 def fwd(q, k, v, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=0, block_mask=None,
-        scale=None, return_o_f32=False, stream=None, prof=None, window=0, out=None, workspace=None):
+        scale=None, return_o_f32=False, stream=None, prof=None, window=0, out=None, workspace=None, fwd_kernel=0):
     """O, LSE (and optionally the float32 O before rounding) via fa_fwd.
 
     k, v may have fewer heads than q (grouped-query attention); ``window`` > 0
     (with ``causal``) restricts query i to keys i - window < j <= i.  ``out``
     = (o, lse) and ``workspace`` (uint8, fa_fwd_workspace_size bytes) let a
-    caller reuse its own buffers instead of allocating on every call."""
+    caller reuse its own buffers instead of allocating on every call.
+    ``fwd_kernel`` (head dimension 64): 0 lets the library choose, 1 / 2
+    force the one- / two-query-tile kernel."""
     _check(q)
     (q,), (k, v) = _layouts([q], [k, v])
     lib = load()
@@ -240,7 +245,7 @@ def fwd(q, k, v, *, causal=False, seqlens_k=None, dropout_p=0.0, seed=0, offset=
     o, lse = _outputs(out, [q, ((B, H, N), torch.float32, q.device)])
     o32 = torch.empty((B, H, N, d), device=q.device, dtype=torch.float32) if return_o_f32 else None
     p = make_params(q, k=k, causal=causal, seqlens_k=seqlens_k, dropout_p=dropout_p, seed=seed, offset=offset,
-                    block_mask=block_mask, scale=scale, o_f32=o32, prof=prof, window=window)
+                    block_mask=block_mask, scale=scale, o_f32=o32, prof=prof, window=window, fwd_kernel=fwd_kernel)
     wsz = lib.fa_fwd_workspace_size(ctypes.byref(p))
     ws = _workspace(wsz, workspace, q.device)
     st = lib.fa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), wsz, _stream(stream))

@@ -298,6 +298,7 @@ fa_status fa_fwd(const fa_params* p, const void* q, const void* k, const void* v
   a.scale_log2 = scale_of(p) * 1.4426950408889634f;
   a.mask = mask_of(p, L, w);
   a.drop = dropout_of(p);
+  a.fwd_kernel = p->fwd_kernel;
   a.lse = lse;
   a.o_f32 = p->o_f32;
   a.status = reinterpret_cast<int*>(w + L.status);
@@ -514,6 +515,6 @@ const char* fa_status_string(fa_status s) {
   return "FA_ERR_UNKNOWN";
 }
 
-int32_t fa_version(void) { return 102; }
+int32_t fa_version(void) { return 103; }
 
 }  // extern "C"

@@ -58,6 +58,7 @@ struct FwdArgs {
   float* o_f32;               // optional [B,H,N,64]
   int* status;
   Fp8Args f8;                 // FP8 forward only
+  int fwd_kernel;             // head dim 64: 0 = library's choice, 1 = one query tile per CTA, 2 = two
 };
 
 // Quantiser of the FP8 forward: Q, K and V rows (optionally rotated) to E4M3
@@ -100,6 +101,9 @@ struct BwdArgs {
 // d: head dimension, 64 or 128
 cudaError_t launch_fwd_tc(int dtype, int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& o, const FwdArgs& a, cudaStream_t s);
+// Head dimension 64: one query tile per CTA, two CTAs per SM.
+cudaError_t launch_fwd_tc1(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                           const CUtensorMap& o, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_tc(int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a, cudaStream_t s);
 // Head dimension 128 (Q, dO and the dQ accumulator maps have 64-row boxes).

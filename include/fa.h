@@ -107,6 +107,14 @@ typedef struct {
   int64_t kv_stride_n;       /* when H_kv == H                                  */
   int32_t window;            /* w > 0: key j visible to query i only if
                                 i - w < j (requires causal); 0 = no window     */
+  /* -- ABI 1.3 -- zero-filled by older callers, which keeps their meaning */
+  int32_t fwd_kernel;        /* forward kernel at head dimension 64:
+                                0 = chosen by the library (see fa_fwd);
+                                1 = one 128-row query tile per CTA, two CTAs
+                                    per SM; 2 = two query tiles per CTA
+                                    sharing their K/V tiles.  Both compute
+                                    the same result; other values and other
+                                    head dimensions ignore it             */
 } fa_params;
 
 /* ---------------------------------------------------------------------------
@@ -138,6 +146,10 @@ size_t fa_bwd_workspace_size(const fa_params *p);
  * Philox4x32-10(counter = (j>>3, (b*H+h)*N+i, lo32(offset), hi32(offset)),
  * key = (lo32(seed), hi32(seed))) is >= round(p * 65536); slice t is half
  * (t & 1) of output word (t >> 1), low half first.  Requires B*H*N < 2^32.
+ * At head dimension 64 with fwd_kernel = 0 the library runs the one-tile
+ * kernel unless the query tiles average at least 64 key tiles (dense or
+ * causal, no window, no block mask) and the two-tile grid fills at least four
+ * waves of the GPU, where sharing K/V tiles between two query tiles wins.
  * ------------------------------------------------------------------------- */
 fa_status fa_fwd(const fa_params *p, const void *q, const void *k, const void *v,
                  void *o, float *lse, void *ws, size_t ws_bytes, void *stream);
@@ -307,7 +319,8 @@ fa_status fa_fwd_fp8(const fa_params *p, const fa_fp8_params *f, const void *buf
 const char *fa_status_string(fa_status s);
 
 /* Library ABI version (major * 100 + minor): 101 adds H_kv, kv_stride_*
- * and window to fa_params; 102 adds the FP8 forward. */
+ * and window to fa_params; 102 adds the FP8 forward; 103 adds fwd_kernel,
+ * fa_noalloc_check_status and fa_noalloc_scratch. */
 int32_t fa_version(void);
 
 #ifdef __cplusplus

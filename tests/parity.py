@@ -74,15 +74,18 @@ def kwargs_of(wl: W.Workload):
                 window=wl.window)
 
 
-def run_gpu(wl: W.Workload, inputs, layout="bhnd", want_o32=True):
-    """fwd + bwd through the C ABI; returns numpy float64 copies of everything."""
+def run_gpu(wl: W.Workload, inputs, layout="bhnd", want_o32=True, fwd_kernel=0):
+    """fwd + bwd through the C ABI; returns numpy float64 copies of everything.
+
+    fwd_kernel selects the head-dimension-64 forward kernel (0: the library's
+    choice, 1: one query tile per CTA, 2: two query tiles per CTA)."""
     dev = torch.device("cuda:0")
     t = {k: v.to(dev) for k, v in inputs.items()}
     if layout == "bnhd":   # non-contiguous strides: [B, N, H, d] memory viewed as [B, H, N, d]
         t = {k: v.transpose(1, 2).contiguous().transpose(1, 2) for k, v in t.items()}
     kw = kwargs_of(wl)
     want_o32 = want_o32 and wl.dtype != "f32"
-    out = fa.fwd(t["q"], t["k"], t["v"], return_o_f32=want_o32, **kw)
+    out = fa.fwd(t["q"], t["k"], t["v"], return_o_f32=want_o32, fwd_kernel=fwd_kernel, **kw)
     o, lse = out[0], out[1]
     st = fa.check_status(fa.fwd.last_workspace)
     assert st == 0, "fa_fwd device status %d" % st

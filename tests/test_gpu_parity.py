@@ -28,9 +28,9 @@ def _wl(N, dtype="bf16", B=2, H=3, seed=7, **kw):
     return W.Workload("case", B=B, H=H, N=N, dtype=dtype, seed=seed, **kw)
 
 
-def _check_all_heads(wl, layout="bhnd"):
+def _check_all_heads(wl, layout="bhnd", fwd_kernel=0):
     inp = W.make_inputs(wl)
-    got = run_gpu(wl, inp, layout=layout)
+    got = run_gpu(wl, inp, layout=layout, fwd_kernel=fwd_kernel)
     worst = {}
     for b in range(wl.B):
         for h in range(wl.H):
@@ -166,3 +166,46 @@ def test_rescale_decided_per_row_within_a_warp():
         got = run_gpu(w, inp)
         for h in range(w.H):
             check_head(w, inp, got, 0, h)
+
+
+# ---- both head-dimension-64 forward kernels.  The library picks the one-tile
+# kernel for every case above; these force each kernel on the same mask mix.
+TWO_KERNEL_CASES = {
+    "dense_ragged_f16": dict(N=300, dtype="f16"),
+    "causal_bf16": dict(N=513, causal=True),
+    "padding_dropout": dict(N=384, B=2, H=2, causal=True, dropout_p=0.2, seqlens=np.array([200, 384], dtype=np.int32)),
+    "empty_rows": dict(N=300, B=4, H=2, seqlens=np.array([0, 1, 300, 157], dtype=np.int32)),
+    "gqa_window": dict(N=384, B=2, H=4, H_kv=2, causal=True, window=150),
+    "sparse_causal": dict(N=1024, B=1, H=2, sparse_butterfly=True, causal=True),
+}
+
+
+@pytest.mark.parametrize("fwd_kernel", [1, 2])
+@pytest.mark.parametrize("case", sorted(TWO_KERNEL_CASES))
+def test_both_d64_forward_kernels(case, fwd_kernel):
+    _check_all_heads(_wl(**TWO_KERNEL_CASES[case]), fwd_kernel=fwd_kernel)
+
+
+@pytest.mark.parametrize("fwd_kernel", [1, 2])
+def test_both_d64_forward_kernels_rescale_and_strides(fwd_kernel):
+    wl = _wl(256, "bf16", B=1, H=2, seed=13)
+    inp = W.make_inputs(wl)
+    qs = torch.where(torch.arange(256) % 2 == 0, 4.0, 0.1).view(1, 1, 256, 1)
+    ks = torch.where(torch.arange(256) < 128, 0.1, 4.0).view(1, 1, 256, 1)
+    inp["q"] = (inp["q"].float() * qs).to(torch.bfloat16)
+    inp["k"] = (inp["k"].float() * ks).to(torch.bfloat16)
+    for w in (wl, wl.with_(causal=True)):
+        got = run_gpu(w, inp, fwd_kernel=fwd_kernel)
+        for h in range(w.H):
+            check_head(w, inp, got, 0, h)
+    _check_all_heads(_wl(200, "bf16", causal=True), layout="bnhd", fwd_kernel=fwd_kernel)
+
+
+def test_d64_forward_kernels_agree_bit_for_bit():
+    """Both kernels run the same per-row arithmetic in the same order, so O
+    and the logsumexp agree exactly."""
+    wl = _wl(640, "bf16", B=2, H=3, causal=True, dropout_p=0.1)
+    inp = W.make_inputs(wl, grads=False)
+    a = run_gpu(wl, inp, fwd_kernel=1)
+    b = run_gpu(wl, inp, fwd_kernel=2)
+    assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
