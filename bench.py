@@ -674,8 +674,10 @@ def _source_hash(which):
     csrc = os.path.join(ROOT, "exact_io_aware_tiled_gb300", "csrc")
     if which == "fwd_fp8":
         files = ["fwd_fp8.cu", "fp8.cuh", "fwd_plan.cuh", "common.cuh"]
+    elif which == "fwd":
+        files = ["fwd_tc.cu", "fwd_tc1.cu", "fwd_plan.cuh", "common.cuh"]
     else:
-        files = ["%s_tc.cu" % which, "common.cuh"] + (["bwd_items.cuh"] if which == "bwd" else [])
+        files = ["bwd_tc.cu", "common.cuh", "bwd_items.cuh"]
     for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             m.update(fh.read())
