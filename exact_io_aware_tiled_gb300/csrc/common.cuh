@@ -424,6 +424,14 @@ template <> struct Cvt<__nv_bfloat16> {
   }
   static __device__ __forceinline__ float lo(uint32_t u) { return __uint_as_float(u << 16); }
   static __device__ __forceinline__ float hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+  // a0 += lo(u), a1 += hi(u): each 16-bit half widened exactly and added in
+  // float32, round to nearest (one mixed-precision add per lane; the same
+  // result as widening first and adding in float32)
+  static __device__ __forceinline__ void acc2(float& a0, float& a1, uint32_t u) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(a0), "+f"(a1) : "r"(u));
+  }
   static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
   static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
   static constexpr int kAB = 1;
@@ -438,6 +446,11 @@ template <> struct Cvt<__half> {
   }
   static __device__ __forceinline__ float hi(uint32_t u) {
     return __half2float(__ushort_as_half((unsigned short)(u >> 16)));
+  }
+  static __device__ __forceinline__ void acc2(float& a0, float& a1, uint32_t u) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
+        : "+f"(a0), "+f"(a1) : "r"(u));
   }
   static __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
   static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }

@@ -336,7 +336,7 @@ fwd_tc1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           const float p0 = ex2(x0), p1 = ex2(x1);
           add2(lt[2 * ch], lt[2 * ch + 1], p0, p1);
           uint32_t u = kDrop ? Cvt<T>::pack(p0 * pscale, p1 * pscale) : Cvt<T>::pack(p0, p1);
-          add2(lr[2 * ch], lr[2 * ch + 1], Cvt<T>::lo(u), Cvt<T>::hi(u));
+          Cvt<T>::acc2(lr[2 * ch], lr[2 * ch + 1], u);
           if constexpr (kDrop) {
             const uint32_t kb = keep[c >> 5] >> (c & 31);
             u &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
