@@ -541,15 +541,19 @@ class Runner:
         dq, dk, dv = fa.bwd(src["q"], src["k"], src["v"], o, src["do"], lse, prof=prof_b, **self.kw)
         return o, lse, dq
 
-    def warmup(self, n):
-        fa, torch = self.fa, self.torch
-        for _ in range(n):
-            self.step()
-        torch.cuda.synchronize()
+    def check_status(self, when):
+        """Exit if the last forward / backward left an error in its status word."""
+        fa = self.fa
         st_f = fa.check_status(fa.fwd_fp8.last_workspace if self.fp8 else fa.fwd.last_workspace)
         st_b = 0 if self.fp8 else fa.check_status(fa.bwd.last_workspace)
         if st_f or st_b:
-            raise SystemExit("device status after warm-up (%s): fwd %d bwd %d" % (self.wl.name, st_f, st_b))
+            raise SystemExit("device status after %s (%s): fwd %d bwd %d" % (when, self.wl.name, st_f, st_b))
+
+    def warmup(self, n):
+        for _ in range(n):
+            self.step()
+        self.torch.cuda.synchronize()
+        self.check_status("warm-up")
 
     def _events(self, n):
         torch = self.torch
@@ -586,6 +590,7 @@ class Runner:
             torch.cuda.synchronize()
             steps = [a.elapsed_time(b) for a, b in marks]
             ms = sum(steps) / K
+        self.check_status("the timed steps")
         fw = [e[0].elapsed_time(e[1]) for e in ev[:K]]
         bw = [0.0 if self.fp8 else e[2].elapsed_time(e[3]) for e in ev[:K]]
         return ms, sum(fw) / K, sum(bw) / K, dict(step=steps, fwd=fw, bwd=bw)

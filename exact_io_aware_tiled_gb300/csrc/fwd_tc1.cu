@@ -152,14 +152,33 @@ fwd_tc1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     bars->abort = 0;
     fence_mbar_init();
   }
+  __syncthreads();
+  // Tensor memory: warp 5 allocates it, and only the warps that use it (the
+  // softmax warps 0-3 and the MMA issuers 5 and 6: 192 threads) meet on named
+  // barrier 2 to read its address.  The TMA producer does not wait for the
+  // allocation, so its first loads (Q, then K(0), from HBM / L2 with a latency
+  // of about a microsecond) overlap it.
   if (warp == 5) {
     tmem_alloc(&bars->tmem_base, 256);
     tmem_relinquish();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
+  uint32_t tmem = 0;
+  auto tmem_ready = [&]() {
+    if constexpr (!kDrop) {
+      tc_fence_before();
+      named_bar_sync(2, 192);
+      tc_fence_after();
+      tmem = bars->tmem_base;
+    }
+  };
+  if constexpr (kDrop) {
+    // With dropout (Philox-bound steps) the early start measured slower
+    // (2-3 % at BERT-large sizes): every warp waits for the allocation.
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tmem = bars->tmem_base;
+  }
   constexpr int ab = Cvt<T>::kAB;
   // Register split of the 256 x 128 launch budget (two CTAs per SM): the
   // softmax warpgroup holds a whole 128-column score row per thread; the
@@ -171,17 +190,18 @@ fwd_tc1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     if (warp == 4) {
       // ===================== TMA producer =====================
       if (lane == 0 && n > 0) {
-        prefetch_tmap(&tmQ);
-        prefetch_tmap(&tmK);
-        prefetch_tmap(&tmV);
         mbar_expect_tx(&bars->q_full, TB);
         tma_load_4d(smem + C::kQ, &tmQ, &bars->q_full, 0, qt * kTile, h, b);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
         bool ok = true;
         for (int s = 0; s < n && ok; ++s) {
           const int st = s % NS;
           const uint32_t ph = (uint32_t)(s / NS) & 1u;
           const int kv = tile.kv<kWin>(s);
-          if (!(ok = mbar_wait(&bars->k_empty[st], ph ^ 1u, ctl) && mbar_wait(&bars->v_empty[st], ph ^ 1u, ctl)))
+          // a stage's first use needs no wait
+          if (s >= NS &&
+              !(ok = mbar_wait(&bars->k_empty[st], ph ^ 1u, ctl) && mbar_wait(&bars->v_empty[st], ph ^ 1u, ctl)))
             break;
           mbar_expect_tx(&bars->k_full[st], TB);
           tma_load_4d(smem + C::kK + st * TB, &tmK, &bars->k_full[st], 0, kv * kTile, hk, b);
@@ -197,6 +217,7 @@ fwd_tc1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       }
     } else if (warp == 5) {
       // ===================== S issuer =====================
+      tmem_ready();
       if (lane == 0 && n > 0) {
         constexpr uint32_t idS = idesc_f16(128, 128, ab, 0, 0);
         const uint64_t qd = sdesc_sw128(smem_u32(smem + C::kQ), 16, 1024);
@@ -220,6 +241,7 @@ fwd_tc1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       }
     } else if (warp == 6) {
       // ===================== PV issuer =====================
+      tmem_ready();
       if (lane == 0 && n > 0) {
         constexpr uint32_t idPV = idesc_f16(128, 64, ab, 0, 1);
         const uint64_t vd0 = sdesc_sw128(smem_u32(smem + C::kV), 16384, 1024);
@@ -244,6 +266,7 @@ fwd_tc1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     }
   } else {
     regs_inc<208>();
+    tmem_ready();
     // ===================== softmax warps =====================
     const int r = warp * 32 + lane;             // row within the tile = TMEM lane
     const int i = qt * kTile + r;               // global query row
@@ -312,38 +335,53 @@ fwd_tc1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           keep[g >> 2] = (g & 3) == 0 ? bits : (keep[g >> 2] | (bits << ((g & 3) * 8)));
         }
       }
-      // PV(s-1) must be done before O is rescaled and the P columns reused
-      // (it normally is: it was issued while this step's S was being computed)
-      if (s > 0 && !(ok = warp_wait1(&bars->pv_done, (uint32_t)(s - 1) & 1u, ctl))) break;
-      tc_fence_after();
-      // P = exp2(S * tau*log2e - m) in two halves of 64 keys (32 packed words).
-      // l_true sums the unrounded P (for the logsumexp); l_rnd sums exactly the
-      // 16-bit values the PV MMA consumes before dropout zeroes some of them
-      // (P, or P/(1-p) with dropout), so O / l_rnd is a consistently rounded
-      // convex combination of V rows.
+      // P = exp2(S * tau*log2e - m), packed to 16 bits, one pair of keys per
+      // call.  l_true sums the unrounded P (for the logsumexp); l_rnd sums
+      // exactly the 16-bit values the PV MMA consumes before dropout zeroes
+      // some of them (P, or P/(1-p) with dropout), so O / l_rnd is a
+      // consistently rounded convex combination of V rows.
       const float pscale = kDrop ? a.drop.rp : 1.f;
       float lt[4] = {0.f, 0.f, 0.f, 0.f}, lr[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c2 = 0; c2 < 64; c2 += 2) {
-          const int c = hf * 64 + c2;
-          const int ch = (c >> 1) & 1;
-          float x0, x1;
-          fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2,
-               sl2, nmref, nmref);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          add2(lt[2 * ch], lt[2 * ch + 1], p0, p1);
-          uint32_t u = kDrop ? Cvt<T>::pack(p0 * pscale, p1 * pscale) : Cvt<T>::pack(p0, p1);
-          Cvt<T>::acc2(lr[2 * ch], lr[2 * ch + 1], u);
-          if constexpr (kDrop) {
-            const uint32_t kb = keep[c >> 5] >> (c & 31);
-            u &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
-          }
-          pk[c2 >> 1] = u;
+      auto p_pair = [&](int c) -> uint32_t {
+        const int ch = (c >> 1) & 1;
+        float x0, x1;
+        fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2,
+             sl2, nmref, nmref);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        add2(lt[2 * ch], lt[2 * ch + 1], p0, p1);
+        uint32_t u = kDrop ? Cvt<T>::pack(p0 * pscale, p1 * pscale) : Cvt<T>::pack(p0, p1);
+        Cvt<T>::acc2(lr[2 * ch], lr[2 * ch + 1], u);
+        if constexpr (kDrop) {
+          const uint32_t kb = keep[c >> 5] >> (c & 31);
+          u &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
         }
-        tmem_st32(tP + hf * 32, pk);
+        return u;
+      };
+      // PV(s-1) must be done before the P columns are reused and O is
+      // rescaled.  Its chain of eight dependent MMAs (about 1,000 cycles) was
+      // issued at the end of the previous step.  Without dropout the wait
+      // comes after this step's exponentials (the whole packed row is held in
+      // registers), which keeps it off the softmax's path.  With dropout the
+      // Philox words leave no room for that: the wait comes first and P goes
+      // out per half of 64 keys.
+      if constexpr (kDrop) {
+        if (s > 0 && !(ok = warp_wait1(&bars->pv_done, (uint32_t)(s - 1) & 1u, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c2 = 0; c2 < 64; c2 += 2) pk[c2 >> 1] = p_pair(hf * 64 + c2);
+          tmem_st32(tP + hf * 32, pk);
+        }
+      } else {
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int c2 = 0; c2 < 128; c2 += 2) pk[c2 >> 6][(c2 >> 1) & 31] = p_pair(c2);
+        if (s > 0 && !(ok = warp_wait1(&bars->pv_done, (uint32_t)(s - 1) & 1u, ctl))) break;
+        tc_fence_after();
+        tmem_st32(tP, pk[0]);
+        tmem_st32(tP + 32, pk[1]);
       }
       l_true += (lt[0] + lt[1]) + (lt[2] + lt[3]);
       l_rnd += ((lr[0] + lr[1]) + (lr[2] + lr[3])) / pscale;

@@ -201,6 +201,20 @@ def test_both_d64_forward_kernels_rescale_and_strides(fwd_kernel):
     _check_all_heads(_wl(200, "bf16", causal=True), layout="bnhd", fwd_kernel=fwd_kernel)
 
 
+@pytest.mark.parametrize("fwd_kernel", [1, 2])
+def test_forward_grid_order_covers_every_tile(fwd_kernel):
+    """208 heads (16 x 13) of four query tiles, more CTAs than the GPU holds
+    at once: every head's O and logsumexp must match the oracle in full, so
+    no (b, h, query tile) work item is lost or done twice by the grid's
+    order."""
+    wl = _wl(512, "bf16", B=16, H=13, causal=True)
+    inp = W.make_inputs(wl)
+    got = run_gpu(wl, inp, fwd_kernel=fwd_kernel)
+    for b in range(wl.B):
+        for h in range(wl.H):
+            check_head(wl, inp, got, b, h, do_grads=False)
+
+
 def test_d64_forward_kernels_agree_bit_for_bit():
     """Both kernels run the same per-row arithmetic in the same order, so O
     and the logsumexp agree exactly."""
