@@ -339,39 +339,54 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           keep[g >> 2] = (g & 3) == 0 ? bits : (keep[g >> 2] | (bits << ((g & 3) * 8)));
         }
       }
-      // PV(s-1) must be done before O is rescaled and the P columns reused
-      // (it normally is: it was issued while this step's S was being computed)
-      if (s > 0 && !(ok = warp_wait(&bars->pv_done[x], (uint32_t)(s - 1) & 1u, ctl))) break;
-      tc_fence_after();
-      // P = exp2(S * tau*log2e - m) in two halves of 64 keys (32 packed words).
-      // l_true sums the unrounded P (for the logsumexp); l_rnd sums exactly the
-      // 16-bit values the PV MMA consumes before dropout zeroes some of them
-      // (P, or P/(1-p) with dropout), so O / l_rnd is a consistently rounded
-      // convex combination of V rows.
+      // P = exp2(S * tau*log2e - m), packed to 16 bits, one pair of keys per
+      // call.  l_true sums the unrounded P (for the logsumexp); l_rnd sums
+      // exactly the 16-bit values the PV MMA consumes before dropout zeroes
+      // some of them (P, or P/(1-p) with dropout), so O / l_rnd is a
+      // consistently rounded convex combination of V rows.
       const float pscale = kDrop ? a.drop.rp : 1.f;
       // pair accumulators (packed f32x2 adds): two chains each for l_true, l_rnd
       float lt[4] = {0.f, 0.f, 0.f, 0.f}, lr[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c2 = 0; c2 < 64; c2 += 2) {
-          const int c = hf * 64 + c2;
-          const int ch = (c >> 1) & 1;       // which of the two accumulator chains
-          float x0, x1;
-          fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2,
-               sl2, nmref, nmref);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          add2(lt[2 * ch], lt[2 * ch + 1], p0, p1);
-          uint32_t u = kDrop ? Cvt<T>::pack(p0 * pscale, p1 * pscale) : Cvt<T>::pack(p0, p1);
-          Cvt<T>::acc2(lr[2 * ch], lr[2 * ch + 1], u);
-          if constexpr (kDrop) {
-            const uint32_t kb = keep[c >> 5] >> (c & 31);
-            u &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
-          }
-          pk[c2 >> 1] = u;
+      auto p_pair = [&](int c) -> uint32_t {
+        const int ch = (c >> 1) & 1;       // which of the two accumulator chains
+        float x0, x1;
+        fma2(x0, x1, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2,
+             sl2, nmref, nmref);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        add2(lt[2 * ch], lt[2 * ch + 1], p0, p1);
+        uint32_t u = kDrop ? Cvt<T>::pack(p0 * pscale, p1 * pscale) : Cvt<T>::pack(p0, p1);
+        Cvt<T>::acc2(lr[2 * ch], lr[2 * ch + 1], u);
+        if constexpr (kDrop) {
+          const uint32_t kb = keep[c >> 5] >> (c & 31);
+          u &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
         }
-        tmem_st32(tP + hf * 32, pk);
+        return u;
+      };
+      // PV(s-1) must be done before O is rescaled and the P columns reused.
+      // At D = 64 without dropout the exponentials go into registers first
+      // and the wait comes only before P is stored, after them (the chain of
+      // eight dependent PV MMAs, issued at the end of the previous step, then
+      // stays off the softmax's path).  At D = 128 P lies over S, so PV(s-1)
+      // is done before S(s) exists; with dropout the Philox words leave no
+      // registers for a whole packed row.
+      if constexpr (D == 64 && !kDrop) {
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int c2 = 0; c2 < 128; c2 += 2) pk[c2 >> 6][(c2 >> 1) & 31] = p_pair(c2);
+        if (s > 0 && !(ok = warp_wait(&bars->pv_done[x], (uint32_t)(s - 1) & 1u, ctl))) break;
+        tc_fence_after();
+        tmem_st32(tP, pk[0]);
+        tmem_st32(tP + 32, pk[1]);
+      } else {
+        if (s > 0 && !(ok = warp_wait(&bars->pv_done[x], (uint32_t)(s - 1) & 1u, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c2 = 0; c2 < 64; c2 += 2) pk[c2 >> 1] = p_pair(hf * 64 + c2);
+          tmem_st32(tP + hf * 32, pk);
+        }
       }
       l_true += (lt[0] + lt[1]) + (lt[2] + lt[3]);
       l_rnd += ((lr[0] + lr[1]) + (lr[2] + lr[3])) / pscale;
