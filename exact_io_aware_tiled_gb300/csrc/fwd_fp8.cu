@@ -329,13 +329,15 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       l_run *= alpha;
       const float nmref = (m_run == -INFINITY) ? 0.f : -m_run;
 
-      // PV(s-1) must be done before O is rescaled and the P tile rewritten
-      if (s > 0 && !(ok = warp_wait(&bars->pv_done[x], (uint32_t)(s - 1) & 1u, ctl))) break;
-      tc_fence_after();
+      // The E4M3 codes of the whole row go into registers first; PV(s-1)
+      // must be done before the P tile is rewritten and O rescaled, and the
+      // wait for it comes only then, after this step's exponentials (its
+      // chain of dependent MMAs, issued at the end of the previous step, stays
+      // off the softmax's path).
       float lt[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t w[8][4];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {             // 16 keys (one 16-byte chunk) at a time
-        uint32_t w[4];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int c = j * 16 + q4 * 4;
@@ -349,12 +351,16 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           add2(lt[(q4 & 1) * 2], lt[(q4 & 1) * 2 + 1], p2, p3);
           mul2(p0, p1, p0, p1, ct, ct);
           mul2(p2, p3, p2, p3, ct, ct);
-          w[q4] = e4m3x4(p0, p1, p2, p3);
+          w[j][q4] = e4m3x4(p0, p1, p2, p3);
         }
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                     :: "r"(prow + (((uint32_t)(j ^ r) & 7u) << 4)), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                     : "memory");
       }
+      if (s > 0 && !(ok = warp_wait(&bars->pv_done[x], (uint32_t)(s - 1) & 1u, ctl))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(prow + (((uint32_t)(j ^ r) & 7u) << 4)), "r"(w[j][0]), "r"(w[j][1]), "r"(w[j][2]),
+                        "r"(w[j][3]) : "memory");
       l_run += (lt[0] + lt[1]) + (lt[2] + lt[3]);
       fence_proxy_async_smem();   // the P tile is read by the tensor core (async proxy)
       // tcgen05.ld / st are warp-collective: the warp rescales together when
