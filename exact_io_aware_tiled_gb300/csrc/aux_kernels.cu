@@ -48,7 +48,7 @@ template <typename T>
 __global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ dout, Strides st,
                                 const float* __restrict__ lse, int B, int H, int N, int npad, int dh,
                                 float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dqacc,
-                                int* __restrict__ sched) {
+                                int* __restrict__ sched, float dscale) {
   if (sched != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;   // backward work counter
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 3;
   const int part = threadIdx.x & 7;
@@ -79,7 +79,7 @@ __global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ d
       l2 = (v == -INFINITY) ? INFINITY : v * kLog2e;
     }
     lse2[row] = l2;
-    dvec[row] = i < N ? d : 0.f;
+    dvec[row] = i < N ? d * dscale : 0.f;
   }
 }
 
@@ -155,19 +155,20 @@ __global__ void dropout_mask_kernel(DropoutArgs d, int H, int N, int b, int h, i
 
 cudaError_t launch_bwd_prep(int dtype, const void* o, const void* dout, Strides st, const float* lse, int B, int H,
                             int N, int npad, int d, float* lse2, float* dvec, float* dqacc, int* sched,
-                            cudaStream_t s) {
+                            float dscale, cudaStream_t s) {
   const long long rows = (long long)B * H * npad;
   const int threads = 256;
   const long long blocks = (rows * 8 + threads - 1) / threads;
   if (dtype == FA_DT_BF16)
     bwd_prep_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, s>>>(
-        (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, st, lse, B, H, N, npad, d, lse2, dvec, dqacc, sched);
+        (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, st, lse, B, H, N, npad, d, lse2, dvec, dqacc, sched,
+        dscale);
   else if (dtype == FA_DT_F16)
     bwd_prep_kernel<__half><<<(unsigned)blocks, threads, 0, s>>>((const __half*)o, (const __half*)dout, st, lse, B,
-                                                                 H, N, npad, d, lse2, dvec, dqacc, sched);
+                                                                 H, N, npad, d, lse2, dvec, dqacc, sched, dscale);
   else
     bwd_prep_kernel<float><<<(unsigned)blocks, threads, 0, s>>>((const float*)o, (const float*)dout, st, lse, B, H,
-                                                                N, npad, d, lse2, dvec, dqacc, sched);
+                                                                N, npad, d, lse2, dvec, dqacc, sched, dscale);
   return cudaGetLastError();
 }
 

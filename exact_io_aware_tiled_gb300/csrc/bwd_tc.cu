@@ -47,16 +47,18 @@
 //     of every key row (= tensor-memory lane):
 //       part 1: P from S^T, P~^T (16 bit) into tensor memory for dV;
 //       part 2: dS from dP^T, dS^T (16 bit) into a swizzled shared tile
-//               that both dK and dQ read;
-//       drain:  16 of the 64 columns of dQ_i from tensor memory -> x tau ->
-//               shared staging (in the following step);
-//       item end: 16 of the 64 columns of dK (x tau) and dV from tensor
-//               memory straight to global memory.
+//               that both dK and dQ read (bf16: tau dS, so that dK and dQ
+//               come out scaled);
+//       drain:  16 of the 64 columns of dQ_i from tensor memory (x tau for
+//               fp16) -> shared staging (in the following step);
+//       item end: 16 of the 64 columns of dK (x tau for fp16) and dV from
+//               tensor memory straight to global memory.
 // Tensor memory (512 columns):
 //   S^T 0-127 | dP^T 128-255 | dK 256-319 | dV 320-383 | dQ 384-447 |
 //   P~^T (16 bit, queries 32w..32w+31 packed at 448+16w .. +16) 448-511.
 // Registers: 96 a thread (640 threads, one CTA per SM).
 #include <algorithm>
+#include <type_traits>
 
 #include "bwd_items.cuh"
 
@@ -107,6 +109,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmDQ, const BwdArgs a) {
   using L = BwdSmem;
+  // bf16: tau is folded into dS (the D rows hold -tau * D, and part 2 forms
+  // (tau dP - tau D) o P with one packed FMA), so dQ and dK leave the tensor
+  // core already scaled.  At the usual tau = 2^-3 that is exact.  Not for
+  // fp16, whose smaller range would push small dS values into subnormals.
+  constexpr bool kFold = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   BBars* bars = reinterpret_cast<BBars*>(smem + L::kBar);
@@ -392,7 +399,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int pc_base = (wg & 1) * 4;
     bool ok = true;
 
-    // dQ_t: 16 of its 64 columns, tensor memory -> x tau -> staging buffer t % NSTG
+    // dQ_t: 16 of its 64 columns, tensor memory -> x tau (fp16; bf16 is
+    // already scaled) -> staging buffer t % NSTG
     // (warp 16 reduces it)
     auto drain_dq = [&](int t) -> bool {
       if (!warp_wait(&bars->dq_full, (uint32_t)t & 1u, ctl)) return false;
@@ -406,13 +414,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const int bi = t % NSTG;
       if (t >= NSTG && !warp_wait(&bars->stg_free[bi], (uint32_t)((t - NSTG) / NSTG) & 1u, ctl)) return false;
       uint8_t* sb = smem + L::kDQ + bi * 32768 + (wg >> 1) * 16384 + r * 128;
+      if constexpr (!kFold) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) g[e] = __float_as_uint(__uint_as_float(g[e]) * a.scale);
+      }
 #pragma unroll
       for (int pc4 = 0; pc4 < 4; ++pc4) {
         const uint32_t off = ((((pc_base + pc4) ^ r) & 7) << 4);
-        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
-                     :: "r"(smem_u32(sb + off)),
-                        "f"(__uint_as_float(g[pc4 * 4]) * a.scale), "f"(__uint_as_float(g[pc4 * 4 + 1]) * a.scale),
-                        "f"(__uint_as_float(g[pc4 * 4 + 2]) * a.scale), "f"(__uint_as_float(g[pc4 * 4 + 3]) * a.scale)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(smem_u32(sb + off)), "r"(g[pc4 * 4]), "r"(g[pc4 * 4 + 1]), "r"(g[pc4 * 4 + 2]),
+                        "r"(g[pc4 * 4 + 3])
                      : "memory");
       }
       fence_proxy_async_smem();
@@ -421,7 +432,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     };
 
 
-    // dK (x tau) and dV of an item: 16 of the 64 columns of this thread's key
+    // dK (x tau for fp16) and dV of an item: 16 of the 64 columns of this thread's key
     // row, straight from registers to global memory (32 bytes each).
     auto store_dkv = [&](const Item& it, const uint32_t (&kraw)[16], const uint32_t (&vraw)[16], bool have) {
       const int j = it.jt * kTile + r;
@@ -430,8 +441,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       uint32_t wk[8], wv[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        wk[c] = Cvt<T>::pack(have ? __uint_as_float(kraw[2 * c]) * a.scale : 0.f,
-                             have ? __uint_as_float(kraw[2 * c + 1]) * a.scale : 0.f);
+        const float ks = kFold ? 1.f : a.scale;   // bf16: dK is already scaled
+        wk[c] = Cvt<T>::pack(have ? __uint_as_float(kraw[2 * c]) * ks : 0.f,
+                             have ? __uint_as_float(kraw[2 * c + 1]) * ks : 0.f);
         wv[c] = Cvt<T>::pack(have ? __uint_as_float(vraw[2 * c]) : 0.f, have ? __uint_as_float(vraw[2 * c + 1]) : 0.f);
       }
       if (a.dkv_v8) {
@@ -593,8 +605,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             const uint32_t w0 = pp[cc / 2], w1 = pp[cc / 2 + 1];
             float y[4];
-            sub2(y[0], y[1], g[0], g[1], d4.x, d4.y);
-            sub2(y[2], y[3], g[2], g[3], d4.z, d4.w);
+            if constexpr (kFold) {      // d4 holds -tau * D
+              fma2(y[0], y[1], g[0], g[1], a.scale, a.scale, d4.x, d4.y);
+              fma2(y[2], y[3], g[2], g[3], a.scale, a.scale, d4.z, d4.w);
+            } else {
+              sub2(y[0], y[1], g[0], g[1], d4.x, d4.y);
+              sub2(y[2], y[3], g[2], g[3], d4.z, d4.w);
+            }
             mul2(y[0], y[1], y[0], y[1], Cvt<T>::lo(w0), Cvt<T>::hi(w0));
             mul2(y[2], y[3], y[2], y[3], Cvt<T>::lo(w1), Cvt<T>::hi(w1));
             dsw[q4 * 2] = Cvt<T>::pack(y[0], y[1]);
