@@ -350,10 +350,10 @@ fa_status fa_bwd(const fa_params* p, const void* q, const void* k, const void* v
   if ((s = prepare_common(p, L, w, st)) != FA_OK) return s;
   float* dqacc = p->dtype == FA_DT_F32 ? nullptr : reinterpret_cast<float*>(w + L.dqacc);
   a.sched = reinterpret_cast<int*>(w + L.sched);
-  // The bf16 d = 64 backward folds tau into dS (dS' = (tau dP - tau D) o P
-  // with one packed FMA against -tau D), so its dQ, dK products come out
-  // scaled; every other kernel reads D itself.
-  const float dscale = (p->dtype == FA_DT_BF16 && p->d == 64) ? -a.scale : 1.f;
+  // The bf16 backward kernels fold tau into dS (dS' = (tau dP - tau D) o P
+  // with one packed FMA against -tau D), so their dQ, dK products come out
+  // scaled; the fp16 and fp32 kernels read D itself.
+  const float dscale = p->dtype == FA_DT_BF16 ? -a.scale : 1.f;
   cudaError_t e = launch_bwd_prep(p->dtype, o, dout, sd, lse, p->B, p->H, p->N, L.npad, p->d,
                                   reinterpret_cast<float*>(w + L.lse2), reinterpret_cast<float*>(w + L.dvec), dqacc,
                                   a.sched, dscale, st);

@@ -32,6 +32,7 @@
 // here) have one buffer each; Q, dO and their LSE / D rows a three-stage
 // ring.  Warps 0-15 are four warpgroups of 16 query columns each.
 #include <algorithm>
+#include <type_traits>
 
 #include "bwd_items.cuh"
 
@@ -94,6 +95,11 @@ bwd_tc128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                  const __grid_constant__ CUtensorMap tmDQ, const BwdArgs a) {
   using L = Smem128;
+  // bf16: tau is folded into dS (the D rows hold -tau * D, and part 2 forms
+  // (tau dP - tau D) o P with one packed FMA), so dQ and dK leave the tensor
+  // core already scaled.  Not for fp16, whose smaller range would push small
+  // dS values into subnormals.
+  constexpr bool kFold = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars128* bars = reinterpret_cast<Bars128*>(smem + L::kBar);
@@ -364,7 +370,7 @@ bwd_tc128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int c0 = wg * 16;                   // first query column of this warpgroup
     bool ok = true;
 
-    // dQ_t: head dim r of this warpgroup's 16 queries, tensor memory -> x tau
+    // dQ_t: head dim r of this warpgroup's 16 queries, tensor memory -> x tau (fp16; bf16 is already scaled)
     // -> float32 staging box r / 32 (rows = queries, 32 floats = 128 bytes
     // with the 128-byte swizzle); warp 16 reduces it
     auto drain_dq = [&](int t) -> bool {
@@ -382,15 +388,15 @@ bwd_tc128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       for (int c = 0; c < 16; ++c) {
         const int q = c0 + c;
         const uint32_t off = q * 128 + ((((lane >> 2) ^ q) & 7) << 4) + (lane & 3) * 4;
-        asm volatile("st.shared.f32 [%0], %1;" :: "r"(smem_u32(sb + off)), "f"(__uint_as_float(g[c]) * a.scale)
-                     : "memory");
+        const float v = kFold ? __uint_as_float(g[c]) : __uint_as_float(g[c]) * a.scale;
+        asm volatile("st.shared.f32 [%0], %1;" :: "r"(smem_u32(sb + off)), "f"(v) : "memory");
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars->stg_full);
       return true;
     };
 
-    // dK (x tau) and dV of an item: columns 32 wg .. 32 wg + 31 of this
+    // dK (x tau for fp16) and dV of an item: columns 32 wg .. 32 wg + 31 of this
     // thread's key row, in two halves of 16, straight to global memory
     auto store_dkv = [&](const Item& it, int half, const uint32_t (&kraw)[16], const uint32_t (&vraw)[16],
                          bool have) {
@@ -401,8 +407,9 @@ bwd_tc128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       uint32_t wk[8], wv[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        wk[c] = Cvt<T>::pack(have ? __uint_as_float(kraw[2 * c]) * a.scale : 0.f,
-                             have ? __uint_as_float(kraw[2 * c + 1]) * a.scale : 0.f);
+        const float ks = kFold ? 1.f : a.scale;   // bf16: dK is already scaled
+        wk[c] = Cvt<T>::pack(have ? __uint_as_float(kraw[2 * c]) * ks : 0.f,
+                             have ? __uint_as_float(kraw[2 * c + 1]) * ks : 0.f);
         wv[c] = Cvt<T>::pack(have ? __uint_as_float(vraw[2 * c]) : 0.f, have ? __uint_as_float(vraw[2 * c + 1]) : 0.f);
       }
       if (a.dkv_v8) {
@@ -552,8 +559,13 @@ bwd_tc128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           }
           const uint32_t w0 = pp[q4 * 2], w1 = pp[q4 * 2 + 1];
           float y[4];
-          sub2(y[0], y[1], g[0], g[1], d4.x, d4.y);
-          sub2(y[2], y[3], g[2], g[3], d4.z, d4.w);
+          if constexpr (kFold) {      // d4 holds -tau * D
+            fma2(y[0], y[1], g[0], g[1], a.scale, a.scale, d4.x, d4.y);
+            fma2(y[2], y[3], g[2], g[3], a.scale, a.scale, d4.z, d4.w);
+          } else {
+            sub2(y[0], y[1], g[0], g[1], d4.x, d4.y);
+            sub2(y[2], y[3], g[2], g[3], d4.z, d4.w);
+          }
           mul2(y[0], y[1], y[0], y[1], Cvt<T>::lo(w0), Cvt<T>::hi(w0));
           mul2(y[2], y[3], y[2], y[3], Cvt<T>::lo(w1), Cvt<T>::hi(w1));
           dsw[q4 * 2] = Cvt<T>::pack(y[0], y[1]);

@@ -86,7 +86,7 @@ struct BwdArgs {
   MaskArgs mask;
   DropoutArgs drop;
   const float* lse2;          // [B*H][npad]: LSE*log2(e), +inf for rows without keys / padding
-  const float* dvec;          // [B*H][npad]: D = rowsum(dO o O) (bf16, d = 64: -tau * D), 0 on padding
+  const float* dvec;          // [B*H][npad]: D = rowsum(dO o O) (bf16: -tau * D), 0 on padding
   void* dk;                   // [B,H_kv,N,64] outputs, element strides kst
   void* dv;
   Strides kst;
@@ -118,8 +118,7 @@ cudaError_t launch_bwd_simt(const float* q, const float* k, const float* v, cons
                             cudaStream_t s);
 
 // D = rowsum(dO o O) and the padded LSE*log2e / D arrays; the same pass clears dqacc if given.
-// dvec = dscale * D (the 16-bit d = 64 backward folds -tau into it; see
-// bwd_dvec_scale in api.cu).
+// dvec = dscale * D (the bf16 backward kernels fold -tau into it, see fa_bwd).
 cudaError_t launch_bwd_prep(int dtype, const void* o, const void* dout, Strides st, const float* lse,
                             int B, int H, int N, int npad, int d, float* lse2, float* dvec, float* dqacc,
                             int* sched, float dscale, cudaStream_t s);
