@@ -98,10 +98,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with a suspend-time hint: a thread whose phase is not complete
+// sleeps until it completes or `ns` nanoseconds pass, instead of returning at
+// once, so that a waiting thread takes no issue slots from the warps that are
+// working.  Waking from the sleep is slower than polling, so a kernel chooses
+// (WaitCtl::sleep_ns).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t addr, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(addr), "r"(parity), "r"(ns) : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kWaitSleepNs = 1000000;   // per try: the abort flag and the limit are checked every 32 tries
+
 // Shared state for the bounded-wait abort protocol of one CTA.
 struct WaitCtl {
   int* status;             // global status word (workspace)
   volatile int* abort;     // shared flag: set once any wait in the CTA ran out
+  uint32_t sleep_ns;       // 0: poll; else sleep up to this long per try (see mbar_try_wait_sleep)
 };
 
 // Waits for the phase of `bar` with parity `parity` to complete.  Returns
@@ -115,7 +132,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(a, parity)) return true;
+      if (ctl.sleep_ns ? mbar_try_wait_sleep(a, parity, ctl.sleep_ns) : mbar_try_wait(a, parity)) return true;
     if (*ctl.abort) return false;
     if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
       *ctl.abort = 1;

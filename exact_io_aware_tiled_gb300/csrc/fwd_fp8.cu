@@ -105,7 +105,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   sl[1] = make_slot(a, 2 * pair + 1, Lk);
   const int smax = max(sl[0].n, sl[1].n);
 
-  WaitCtl ctl{a.status, &bars->abort};
+  // The role threads mostly wait on the softmax warps: they sleep while they
+  // wait, leaving the issue slots to the softmax.
+  WaitCtl ctl{a.status, &bars->abort, kWaitSleepNs};
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);

@@ -134,7 +134,9 @@ fwd_tc1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const Tile1 tile = make_tile1(a, qt, Lk);
   const int n = tile.n;
 
-  WaitCtl ctl{a.status, &bars->abort};
+  // The role threads mostly wait on the softmax warps: they sleep while they
+  // wait, leaving the issue slots to the softmax.
+  WaitCtl ctl{a.status, &bars->abort, kWaitSleepNs};
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
