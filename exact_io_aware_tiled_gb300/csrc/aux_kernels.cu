@@ -204,8 +204,9 @@ cudaError_t launch_dropout_mask(const DropoutArgs& d, int H, int N, int b, int h
 }
 
 // Two warps each wait, with the same bounded wait the attention kernels
-// use, on an mbarrier that nothing arrives at.  Warp 1 starts its wait half
-// the limit later than warp 0.  Warp 0's wait runs out first, records
+// use, on an mbarrier that nothing arrives at: warp 0 polling (as in the
+// backward kernels), warp 1 sleeping between tries (as in the forward
+// kernels).  Warp 1 starts its wait half the limit later than warp 0.  Warp 0's wait runs out first, records
 // FA_ERR_TIMEOUT in the status word and raises the CTA abort flag; warp 1's
 // wait then returns on the flag, about half the limit after it started,
 // instead of running its own limit out.  out[w] = 1 if warp w's wait
@@ -220,8 +221,10 @@ __global__ void wait_selftest_kernel(int* status, int* out, unsigned long long* 
     fence_mbar_init();
   }
   __syncthreads();
-  WaitCtl ctl{status, &abort_flag};
   const int w = threadIdx.x >> 5;
+  // warp 0 polls (the backward's waits), warp 1 sleeps between tries (the
+  // forward's): both give up, warp 1 on the abort flag warp 0 raises
+  WaitCtl ctl{status, &abort_flag, w == 1 ? kWaitSleepNs : 0u};
   if ((threadIdx.x & 31) == 0) {
     if (w == 1) {   // a bounded delay of half the wait limit
       const uint64_t d0 = globaltimer_ns();
