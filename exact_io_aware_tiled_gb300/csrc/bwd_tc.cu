@@ -52,7 +52,8 @@
 //       drain:  16 of the 64 columns of dQ_i from tensor memory (x tau for
 //               fp16) -> shared staging (in the following step);
 //       item end: 16 of the 64 columns of dK (x tau for fp16) and dV from
-//               tensor memory straight to global memory.
+//               tensor memory straight to global memory (with dropout:
+//               dK or dV, 16 key rows a warp, as whole 128-byte rows).
 // Tensor memory (512 columns):
 //   S^T 0-127 | dP^T 128-255 | dK 256-319 | dV 320-383 | dQ 384-447 |
 //   P~^T (16 bit, queries 32w..32w+31 packed at 448+16w .. +16) 448-511.
@@ -464,6 +465,72 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       dv[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
     };
 
+    // With dropout, the item end instead has warpgroups 0-1 write dK (x tau
+    // for fp16) and 2-3 write dV, each warp 16 key rows of its lane quarter
+    // (wg & 1 picks which 16).  The 16x256b tensor-memory shape gives each
+    // lane two of every eight columns of two rows; a transpose within each
+    // group of four lanes then gives every lane 32 consecutive bytes, so one
+    // warp store covers eight whole 128-byte rows instead of a 32-byte piece
+    // of 32 rows.  That is faster only when the Philox work fills the compute
+    // warps' issue slots (measured); without dropout the 64 shuffles and
+    // selects a warp adds cost more than the store transactions they save.
+    const bool kv_is_v = wg >= 2;
+    const uint32_t kv_taddr = tmem + ((uint32_t)(quarter * 32 + (wg & 1) * 16) << 16) + (kv_is_v ? kColDV : kColDK);
+    const int kv_row = quarter * 32 + (wg & 1) * 16 + (lane >> 2);   // rows kv_row and kv_row + 8
+    auto store_dkv_rows = [&](const Item& it, const uint32_t (&raw)[32], bool have) {
+      uint32_t w[2][8];     // [row][word]
+      if (have) {
+        const float ks = (!kv_is_v && !kFold) ? a.scale : 1.f;   // bf16: dK is already scaled
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            w[h][k] = Cvt<T>::pack(__uint_as_float(raw[4 * k + 2 * h]) * ks, __uint_as_float(raw[4 * k + 2 * h + 1]) * ks);
+          // w[h][k] belongs at byte 16k + 4 (lane & 3) of its row.  As a 4 x 4
+          // matrix of word pairs (w[2c], w[2c+1]) over the group's lanes, it is
+          // transposed in two exchanges (lane ^ 2, then lane ^ 1), each swapping
+          // the pairs whose column bit differs from the lane's bit.
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int lo = (e >> 1) * 2 + (e & 1), hi = lo + 4;   // pair columns 0/1 against 2/3
+            const bool b1 = lane & 2;
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, b1 ? w[h][lo] : w[h][hi], 2);
+            if (b1) w[h][lo] = got; else w[h][hi] = got;
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int lo = (e >> 1) * 4 + (e & 1), hi = lo + 2;   // pair columns 0/2 against 1/3
+            const bool b0 = lane & 1;
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, b0 ? w[h][lo] : w[h][hi], 1);
+            if (b0) w[h][lo] = got; else w[h][hi] = got;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) w[h][k] = 0u;
+      }
+      // lane q of its group now holds, in pair c, row bytes 32q + 4c (word 0)
+      // and 32q + 16 + 4c (word 1)
+      T* base = static_cast<T*>(kv_is_v ? a.dv : a.dk);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = it.jt * kTile + kv_row + 8 * h;
+        if (j >= a.N) continue;
+        T* p = base + (size_t)it.b * a.kst.b + (size_t)it.hk * a.kst.h + (size_t)j * a.kst.n + (lane & 3) * 16;
+        if (a.dkv_v8) {
+          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                       :: "l"(p), "r"(w[h][0]), "r"(w[h][2]), "r"(w[h][4]), "r"(w[h][6]), "r"(w[h][1]), "r"(w[h][3]),
+                          "r"(w[h][5]), "r"(w[h][7]) : "memory");
+        } else {
+          uint4* q = reinterpret_cast<uint4*>(p);
+          q[0] = make_uint4(w[h][0], w[h][2], w[h][4], w[h][6]);
+          q[1] = make_uint4(w[h][1], w[h][3], w[h][5], w[h][7]);
+        }
+      }
+    };
+
     // the next work item from warp 16's mailbox (-1: none left, or a wait gave up)
     volatile int* item_u = reinterpret_cast<volatile int*>(smem + L::kItem);
     int kc = 0;
@@ -480,9 +547,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     int u;
     while (ok && (u = fetch()) >= 0) {
       const Item it = make_item(a, u);
-      const uint32_t zero[16] = {};
       if (it.steps == 0) {            // no query tile sees this key tile: dK = dV = 0
-        store_dkv(it, zero, zero, false);
+        if constexpr (kDrop) {
+          const uint32_t zero[32] = {};
+          store_dkv_rows(it, zero, false);
+        } else {
+          const uint32_t zero[16] = {};
+          store_dkv(it, zero, zero, false);
+        }
         continue;
       }
       const int j = it.jt * kTile + r;          // global key
@@ -636,17 +708,26 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       // ---- item end: dK, dV out of tensor memory.  The next item's first
       //      dV / dK (which restart the accumulators) follow this thread's
       //      next p_full / ds_full arrivals, hence these loads.
-      uint32_t kraw[16], vraw[16];
       if (!(ok = warp_wait(&bars->dkv_full, (uint32_t)nit & 1u, ctl))) break;
       ++nit;
       tc_fence_after();
-      tmem_ld16(tl + kColDK + wg * 16, kraw);
-      tmem_ld16(tl + kColDV + wg * 16, vraw);
-      tmem_wait_ld();
-      reg_fence16(kraw);
-      reg_fence16(vraw);
-      tc_fence_before();
-      store_dkv(it, kraw, vraw, true);
+      if constexpr (kDrop) {
+        uint32_t raw[32];
+        tmem_ld16x256b_x8(kv_taddr, raw);
+        tmem_wait_ld();
+        reg_fence32(raw);
+        tc_fence_before();
+        store_dkv_rows(it, raw, true);
+      } else {
+        uint32_t kraw[16], vraw[16];
+        tmem_ld16(tl + kColDK + wg * 16, kraw);
+        tmem_ld16(tl + kColDV + wg * 16, vraw);
+        tmem_wait_ld();
+        reg_fence16(kraw);
+        reg_fence16(vraw);
+        tc_fence_before();
+        store_dkv(it, kraw, vraw, true);
+      }
     }
     if (ok && t > 0) ok = drain_dq(t - 1);
   }

@@ -223,3 +223,29 @@ def test_d64_forward_kernels_agree_bit_for_bit():
     a = run_gpu(wl, inp, fwd_kernel=1)
     b = run_gpu(wl, inp, fwd_kernel=2)
     assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dropout_p", [0.0, 0.2])
+def test_backward_outputs_16_byte_aligned(d, dropout_p):
+    """dK and dV written into buffers that start 16 bytes past a 32-byte
+    boundary (their row pieces then leave as 16-byte stores instead of
+    32-byte ones) equal the gradients written into fresh buffers, bit for bit."""
+    g = torch.Generator(device="cuda").manual_seed(11)
+    B, H, N = 2, 2, 300
+    q, k, v, do = (torch.randn((B, H, N, d), device="cuda", generator=g).to(torch.bfloat16) for _ in range(4))
+    kw = dict(causal=True, dropout_p=dropout_p, seed=99, seqlens_k=torch.tensor([300, 170], dtype=torch.int32))
+    o, lse = fa.fwd(q, k, v, **kw)
+    dq0, dk0, dv0 = fa.bwd(q, k, v, o, do, lse, **kw)
+
+    def shifted(like):
+        buf = torch.empty(like.numel() + 8, device="cuda", dtype=like.dtype)
+        t = buf[8:].view(like.shape)             # 16 bytes past the buffer's start
+        assert t.data_ptr() % 32 == 16
+        return t
+
+    dq1 = torch.empty_like(q)
+    dk1, dv1 = shifted(k), shifted(v)
+    fa.bwd(q, k, v, o, do, lse, out=(dq1, dk1, dv1), **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(dq1, dq0) and torch.equal(dk1, dk0) and torch.equal(dv1, dv0)
