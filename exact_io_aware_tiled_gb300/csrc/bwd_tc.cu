@@ -228,6 +228,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         };
         int u;
         while (ok) {
+          // Without dropout the reduce owed here goes before the next item is
+          // claimed, so the producer claims it and issues its first loads only
+          // once the compute threads have drained dQ of the current item's
+          // third-last step.  That later claim was measured faster for short
+          // items (a reduce done first only when already possible was not);
+          // with dropout's longer steps it was slower.
+          if constexpr (!kDrop) {
+            if (!(ok = reduce_to(g - kLag))) break;
+          }
           u = publish();
           if (u < 0) {
             ok = u == -1;

@@ -205,6 +205,13 @@ bwd_tc128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         };
         int u;
         while (ok) {
+          // Without dropout the reduce owed here goes before the next item is
+          // claimed, so the producer claims it and issues its first loads only
+          // once the compute threads have drained dQ of the current item's
+          // third-last step (measured faster at head dimension 64).
+          if constexpr (!kDrop) {
+            if (!(ok = reduce_to(g - kLag))) break;
+          }
           u = publish();
           if (u < 0) {
             ok = u == -1;
