@@ -1,14 +1,16 @@
-"""The d = 64 backward kernel's barrier protocol, simulated on the CPU.
+"""The backward kernels' barrier protocol, simulated on the CPU.
 
-The persistent backward kernel (exact_io_aware_tiled_gb300/csrc/bwd_tc.cu)
-runs five roles that meet only at mbarriers: the TMA producer (which also
+The persistent backward kernels (exact_io_aware_tiled_gb300/csrc/bwd_tc.cu
+at head dimension 64, bwd_tc128.cu at 128) run five roles that meet only at mbarriers: the TMA producer (which also
 claims work items and issues the dQ reduce-adds), the S^T / dP^T issuer, the
 dV / dK issuer, the dQ issuer and the compute warps.  This test restates each
-role's sequence of waits and arrivals as that file issues them (phases by
+role's sequence of waits and arrivals as those files issue them (phases by
 their absolute index, asynchronous completions -- TMA loads and tcgen05
 commits -- as events that fire at some later time) and runs random
 interleavings over random work-item sequences, with and without the
-dropout variant's item-claim order.  It checks that
+dropout variant's item-claim order.  At d = 64, K is double-buffered per item
+and V has a buffer of its own; at d = 128 K and V share one load and one
+buffer, and each 128-row query tile is two 64-row steps.  It checks that
 
 * every run finishes (no interleaving deadlocks);
 * no parity wait could pass early: when a role starts waiting for phase k,
@@ -51,8 +53,9 @@ class Sim:
     """Roles are generators yielding ('wait', bar, k): block until phase k of
     bar is complete (k = -1: the phase before the first, complete at start)."""
 
-    def __init__(self, items, drop, rng, plant=None):
-        self.items, self.drop, self.rng, self.plant = items, drop, rng, plant
+    def __init__(self, items, drop, rng, plant=None, d=64):
+        self.items, self.drop, self.rng, self.plant, self.d = items, drop, rng, plant, d
+        self.per_tile = 1 if d == 64 else 2                               # steps per query tile
         B = Bar
         self.item_full = [B("item_full%d" % i, 1) for i in range(2)]
         self.item_empty = [B("item_empty%d" % i, 4) for i in range(2)]   # three issuers + the compute warps
@@ -60,7 +63,8 @@ class Sim:
         self.k_empty = [B("k_empty%d" % i, 2) for i in range(2)]          # S^T issuer and dQ issuer
         self.q_full = [B("q_full%d" % i, 1) for i in range(NSB)]
         self.q_empty = [B("q_empty%d" % i, 1) for i in range(NSB)]
-        self.v_full, self.v_empty = B("v_full", 1), B("v_empty", 1)
+        self.v_full, self.v_empty = B("v_full", 1), B("v_empty", 1)      # d = 64
+        self.kv_full, self.kv_empty = B("kv_full", 1), B("kv_empty", 2)   # d = 128: S^T / dP^T and dQ issuers
         for n in ("s_full", "p_full", "dp_full", "ds_full", "dq_full", "dq_free", "dkv_full", "pt_free"):
             setattr(self, n, B(n, 1))
         self.dsm_free = B("dsm_free", 2)                                  # dK and dQ read the dS^T tile
@@ -112,13 +116,17 @@ class Sim:
             u = yield from publish()
             if u < 0:
                 break
-            steps = self.items[u]
+            steps = self.items[u] * self.per_tile
             if steps == 0:
                 yield from reduce_to(st["g"] - 3)
                 continue
-            kb = st["nkv"] & 1
-            yield ("wait", self.k_empty[kb], (st["nkv"] >> 1) - 1)
-            self.load(self.k_full[kb])
+            if self.d == 64:
+                kb = st["nkv"] & 1
+                yield ("wait", self.k_empty[kb], (st["nkv"] >> 1) - 1)
+                self.load(self.k_full[kb])
+            else:
+                yield ("wait", self.kv_empty, st["nkv"] - 1)
+                self.load(self.kv_full)
             vi = st["nkv"]
             st["nkv"] += 1
             for t in range(steps):
@@ -131,7 +139,7 @@ class Sim:
                 self.load(self.q_full[g % NSB])
                 self.info[g & 3] = g
                 st["loaded"] = g
-                if t == 0:
+                if t == 0 and self.d == 64:
                     yield ("wait", self.v_empty, vi - 1)
                     self.load(self.v_full)
                 yield from reduce_to(g - KLAG)
@@ -152,11 +160,14 @@ class Sim:
             kc += 1
             if u < 0:
                 break
-            steps = self.items[u]
+            steps = self.items[u] * self.per_tile
             if steps == 0:
                 continue
             kb = nkv & 1
-            yield ("wait", self.k_full[kb], nkv >> 1)
+            if self.d == 64:
+                yield ("wait", self.k_full[kb], nkv >> 1)
+            else:
+                yield ("wait", self.kv_full, nkv)
             vi = nkv
             nkv += 1
             for t in range(steps):
@@ -166,12 +177,15 @@ class Sim:
                 self.commit("S", self.s_full)
                 if g > 0:
                     yield ("wait", self.ds_full, g - 1)
-                if t == 0:
+                if t == 0 and self.d == 64:
                     yield ("wait", self.v_full, vi)
                 self.commit("S", self.dp_full)
                 g += 1
-            self.commit("S", self.k_empty[kb])
-            self.commit("S", self.v_empty)
+            if self.d == 64:
+                self.commit("S", self.k_empty[kb])
+                self.commit("S", self.v_empty)
+            else:
+                self.commit("S", self.kv_empty)
 
     def dvdk_issuer(self):
         g = kc = 0
@@ -180,7 +194,7 @@ class Sim:
             kc += 1
             if u < 0:
                 break
-            steps = self.items[u]
+            steps = self.items[u] * self.per_tile
             if steps == 0:
                 continue
             for t in range(steps):
@@ -200,7 +214,7 @@ class Sim:
             kc += 1
             if u < 0:
                 break
-            steps = self.items[u]
+            steps = self.items[u] * self.per_tile
             if steps == 0:
                 continue
             kb = nkv & 1
@@ -212,7 +226,7 @@ class Sim:
                 self.commit("Q", self.dq_full)
                 self.commit("Q", self.dsm_free)
                 g += 1
-            self.commit("Q", self.k_empty[kb])
+            self.commit("Q", self.k_empty[kb] if self.d == 64 else self.kv_empty)
 
     def compute(self):
         t = nit = kc = 0
@@ -229,7 +243,7 @@ class Sim:
             kc += 1
             if u < 0:
                 break
-            steps = self.items[u]
+            steps = self.items[u] * self.per_tile
             if steps == 0:
                 continue
             for _ in range(steps):
@@ -298,27 +312,30 @@ def _items(rng):
     return [rng.choice([0, 1, 1, 2, 3, 4, 5, 8, 8, 10]) for _ in range(n)]
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("drop", [False, True])
-def test_backward_protocol_never_deadlocks_or_aliases(drop):
-    rng = random.Random(20260 + drop)
+def test_backward_protocol_never_deadlocks_or_aliases(drop, d):
+    rng = random.Random(20260 + drop + d)
     for trial in range(300):
-        Sim(_items(rng), drop, random.Random(rng.random())).run()
+        Sim(_items(rng), drop, random.Random(rng.random()), d=d).run()
 
 
-def test_backward_protocol_single_and_empty_items():
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_protocol_single_and_empty_items(d):
     for items in ([1], [0], [0, 0, 1], [1, 0, 1, 0], [8], [1] * 12, [0] * 5 + [2]):
         for drop in (False, True):
             for seed in range(20):
-                Sim(items, drop, random.Random(seed)).run()
+                Sim(items, drop, random.Random(seed), d=d).run()
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("plant", ["reduce_unstaged", "ring_too_deep"])
-def test_planted_protocol_mistakes_are_caught(plant):
+def test_planted_protocol_mistakes_are_caught(plant, d):
     rng = random.Random(7)
     caught = False
     for trial in range(200):
         try:
-            Sim(_items(rng), False, random.Random(rng.random()), plant=plant).run()
+            Sim(_items(rng), False, random.Random(rng.random()), plant=plant, d=d).run()
         except ProtocolError:
             caught = True
             break
