@@ -29,29 +29,15 @@ import random
 
 import pytest
 
+from tests.protocol_sim import Bar, Engine, ProtocolError
+
 NSB = 3      # Q / dO ring stages
 NSTG = 1     # float32 dQ staging buffers
 KLAG = 3     # the dQ reduce of step g - KLAG follows the loads of step g
 
 
-class ProtocolError(AssertionError):
-    pass
-
-
-class Bar:
-    def __init__(self, name, count):
-        self.name, self.count, self.pending, self.completed = name, count, 0, 0
-
-    def arrive(self):
-        self.pending += 1
-        if self.pending == self.count:
-            self.pending = 0
-            self.completed += 1
-
-
 class Sim:
-    """Roles are generators yielding ('wait', bar, k): block until phase k of
-    bar is complete (k = -1: the phase before the first, complete at start)."""
+    """The five roles of one CTA as generators (tests/protocol_sim.py)."""
 
     def __init__(self, items, drop, rng, plant=None, d=64):
         self.items, self.drop, self.rng, self.plant, self.d = items, drop, rng, plant, d
@@ -72,15 +58,17 @@ class Sim:
         self.stg_free = [B("stg_free%d" % i, 1) for i in range(NSTG)]
         self.mailbox = [None, None]
         self.info = [None] * 4
-        self.fifos = {}
+        self.engine = Engine(rng)
+        self.nloads = 0
 
     # asynchronous arrivals: tcgen05 commits complete in issue order per
     # thread; TMA loads in any order
     def commit(self, who, bar):
-        self.fifos.setdefault(who, []).append(bar)
+        self.engine.later(who, bar)
 
     def load(self, bar):
-        self.fifos.setdefault(("tma", len(self.fifos)), []).append(bar)
+        self.nloads += 1
+        self.engine.later(("tma", self.nloads), bar)
 
     # ------------------------------------------------------------------ roles
     def producer(self):
@@ -264,47 +252,9 @@ class Sim:
         if t > 0:
             yield from drain(t - 1)
 
-    # ------------------------------------------------------------- scheduler
-    def run(self, max_events=10 ** 6):
-        roles = {"P": self.producer(), "S": self.s_issuer(), "D": self.dvdk_issuer(), "Q": self.dq_issuer(),
-                 "C": self.compute()}
-        waiting = {}
-
-        def advance(name):
-            try:
-                req = next(roles[name])
-            except StopIteration:
-                del roles[name]
-                waiting.pop(name, None)
-                return
-            _, bar, k = req
-            if bar.completed < k:
-                raise ProtocolError("%s starts waiting for phase %d of %s while phase %d is incomplete: "
-                                    "the parity wait would pass at once" % (name, k, bar.name, k - 1))
-            waiting[name] = (bar, k)
-
-        for name in list(roles):
-            advance(name)
-        for _ in range(max_events):
-            for name, (bar, k) in waiting.items():
-                if bar.completed > k + 1:
-                    raise ProtocolError("%s waits for phase %d of %s, which is already %d phases on: "
-                                        "the parity aliases" % (name, k, bar.name, bar.completed - k))
-            ready = [n for n, (bar, k) in waiting.items() if bar.completed >= k + 1]
-            fifos = [f for f, q in self.fifos.items() if q]
-            choices = [("role", n) for n in ready] + [("async", f) for f in fifos]
-            if not choices:
-                if roles:
-                    raise ProtocolError("deadlock: %s" % ", ".join(
-                        "%s waits %s phase %d (completed %d)" % (n, b.name, k, b.completed)
-                        for n, (b, k) in waiting.items()))
-                return
-            kind, x = choices[self.rng.randrange(len(choices))]
-            if kind == "role":
-                advance(x)
-            else:
-                self.fifos[x].pop(0).arrive()
-        raise ProtocolError("no end after %d events" % max_events)
+    def run(self):
+        self.engine.run({"P": self.producer(), "S": self.s_issuer(), "D": self.dvdk_issuer(), "Q": self.dq_issuer(),
+                         "C": self.compute()})
 
 
 def _items(rng):
